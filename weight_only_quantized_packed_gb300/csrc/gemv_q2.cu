@@ -1,0 +1,41 @@
+// Ternary Q2_0 scalar-FMA GEMV ("spark_model/layers/ops/gemv_q2_vec.rs":
+// docs of `q2_0_gemv_vec` / `q2_0_gemv_vec_batchm`, test helper `gemv_row`).
+#include "decode.cuh"
+#include "gemv_scalar.cuh"
+
+namespace wqp {
+
+struct Q2Fmt {
+  // One ring stage holds 8 groups (1024 K) of a row: 8 blocks x 34 bytes.
+  static constexpr int kWBytesPerRow = 8 * 34;
+  static constexpr bool kJ8 = true;
+  // Row tiles start at byte 34 * (n * K/128 + 8 t); 16-byte aligned for every
+  // n iff K/128 is a multiple of 8.
+  static bool bulk_ok(int K) { return (K / 128) % 8 == 0; }
+  __device__ static uint32_t row_tile_bytes(int, int, int tg) { return 34u * tg; }
+  __device__ static void issue_row_bulk(const ScalarParams& p, int n, int t, int tg, uint32_t dst,
+                                        uint32_t bar, uint64_t pol) {
+    const size_t G = static_cast<size_t>(p.K >> 7);
+    bulk_g2s_stream(dst, p.W + (n * G + 8 * t) * 34, 34u * tg, bar, pol);
+  }
+  __device__ static void copy_row_plain(const ScalarParams& p, int n, int t, int tg, uint8_t* dst,
+                                        int lane) {
+    const size_t G = static_cast<size_t>(p.K >> 7);
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(p.W + (n * G + 8 * t) * 34);
+    uint16_t* d = reinterpret_cast<uint16_t*>(dst);
+    for (int i = lane; i < 17 * tg; i += 32) d[i] = __ldg(src + i);
+  }
+  // Segment sg of a tile = word (sg % 8) of block (sg / 8): K offset 16 * sg.
+  __device__ static void decode(const ScalarParams&, int, int, int sg, const uint8_t* sW, Seg& g) {
+    const uint8_t* blk = sW + (sg >> 3) * 34;
+    q2_decode_word(q2_code_word(blk, sg & 7), g.p);
+    g.s = q2_scale(blk);
+  }
+};
+
+cudaError_t launch_q2_gemv(const GemvArgs& a, cudaStream_t s) {
+  return Q2Fmt::bulk_ok(a.K) ? launch_scalar_dispatch<Q2Fmt, true>(a, s)
+                             : launch_scalar_dispatch<Q2Fmt, false>(a, s);
+}
+
+}  // namespace wqp

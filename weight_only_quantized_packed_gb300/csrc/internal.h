@@ -1,0 +1,63 @@
+// Internal launch interface between the C-ABI layer (abi.cu) and the kernel
+// translation units. Not installed; the public surface is include/wqp.h.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace wqp {
+
+// Bits of the device error word.
+constexpr unsigned WQP_DEV_ERR_TIMEOUT = 1u;
+
+// One launch computes rows [0, M) of C with 1 <= M <= 16.
+struct GemvArgs {
+  const void* A;        // bf16 [M, lda]
+  const void* W;        // packed weights
+  const void* scales;   // format-specific (NULL for Q2_0)
+  void* C;              // bf16 [M, ldc]
+  int M, N, K;
+  int lda, ldc;         // row pitches in elements
+  float gscale;         // W4 per-tensor scale (1.0 otherwise)
+  unsigned* err;        // device error word
+  int num_sms;
+  bool pdl;             // launch with programmatic stream serialization
+};
+
+struct DequantArgs {
+  const void* W;
+  const void* scales;
+  float* out;           // f32 [N, K]
+  int N, K;
+  float gscale;
+  bool pdl;
+};
+
+cudaError_t launch_q2_gemv(const GemvArgs& a, cudaStream_t s);
+cudaError_t launch_w4a16_gemv(const GemvArgs& a, cudaStream_t s);
+cudaError_t launch_w8a16_gemm(const GemvArgs& a, cudaStream_t s);
+cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s);
+
+cudaError_t launch_q2_dequant(const DequantArgs& a, cudaStream_t s);
+cudaError_t launch_w4a16_dequant(const DequantArgs& a, cudaStream_t s);
+cudaError_t launch_w8a16_dequant(const DequantArgs& a, cudaStream_t s);
+
+// Launch helper: programmatic stream serialization when pdl is set.
+template <typename Kern, typename... Args>
+cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                   Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace wqp
