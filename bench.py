@@ -1,0 +1,519 @@
+"""Benchmark of the packed weight-only-quantized decode GEMV/GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl wqp|reference]
+
+Headline workload: the ternary Q2_0 GEMV at the 27B-class qkv/o projection
+shape, N = K = 5120, with M = 1, 4 and 8 activation rows. One step is three
+calls (M = 1, 4, 8), each on a different weight buffer. The buffers are
+cycled over more than 3x the L2 size, so HBM, not L2, supplies the weights.
+The metric is effective weight-stream bandwidth: packed weight bytes (codes
+plus scales, not A, C or the per-tensor scale) per second. The same line
+reports per-call times for the other workloads (W4A16 at 5120^2, W8A16 for
+the dense-FFN shapes with the scalar and tensor-core paths, and the Q2_0
+decoder-layer sequence), the roofline of the dominant kernel, an end-to-end
+number through the C ABI with host buffers, and the CPU oracle timed on the
+host's cores.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas: the op has no exchange step), and value = all ranks' bytes / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective weight-stream GB/s (% of GB300 HBM peak) and us/call at M=1..16"
+UNIT = "GB/s"
+HEADLINE = {"fmt": "q2", "N": 5120, "K": 5120, "Ms": (1, 4, 8)}
+KERNEL_SOURCES = ["gemv_scalar.cuh", "gemv_q2.cu", "decode.cuh", "common.cuh"]
+
+
+# ------------------------------------------------------------------ helpers
+def weight_bytes(fmt, N, K):
+    from weight_only_quantized_packed_gb300 import synth
+
+    return {"q2": synth.q2_weight_bytes, "w4": synth.w4_weight_bytes,
+            "w8": synth.w8_weight_bytes}[fmt](N, K)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("sm_max_mhz", 2070.0)), "measured"
+    except Exception:
+        return 6800.0, 2070.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while timing."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "weight_only_quantized_packed_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("source_hash") == source_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ GPU arm
+class Workload:
+    """Device-resident inputs for one format/shape, weights cycled over
+    enough buffers to exceed 3x L2."""
+
+    def __init__(self, fmt, N, K, Ms, l2_bytes, seed_workload, tc=False, cap_bytes=3 << 30):
+        import torch
+
+        from tests import _gpu as G
+        from weight_only_quantized_packed_gb300 import synth
+
+        self.fmt, self.N, self.K, self.Ms, self.tc = fmt, N, K, tuple(Ms), tc
+        self.wb = weight_bytes(fmt, N, K)
+        self.nbuf = max(2, min(math.ceil(3 * l2_bytes / self.wb), max(2, cap_bytes // self.wb)))
+        seed = synth.seed_for(seed_workload, 0)
+        if fmt == "q2":
+            W, _, _ = synth.q2_weights(N, K, seed)
+            S = None
+        elif fmt == "w4":
+            W, S, _ = synth.w4_weights(N, K, seed)
+        else:
+            W, S = synth.w8_weights(N, K, seed)
+        w0 = G.dev_u8(W)
+        self.W = [w0] + [w0.clone() for _ in range(self.nbuf - 1)]
+        if S is None:
+            self.S = [None] * self.nbuf
+        else:
+            s0 = G.dev_u8(S) if fmt == "w4" else G.dev_f32(S)
+            self.S = [s0] + [s0.clone() for _ in range(self.nbuf - 1)]
+        self.A = {M: G.dev_bf16(synth.activations(M, K, synth.seed_for(seed_workload, M))) for M in self.Ms}
+        self.C = {M: torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for M in self.Ms}
+        self.i = 0
+
+    def call(self, M, A=None, C=None):
+        import weight_only_quantized_packed_gb300 as wqp
+
+        j = self.i % self.nbuf
+        self.i += 1
+        A = self.A[M] if A is None else A
+        C = self.C[M] if C is None else C
+        if self.fmt == "q2":
+            wqp.q2_gemv(A, self.W[j], self.N, self.K, out=C)
+        elif self.fmt == "w4":
+            wqp.w4a16_gemv(A, self.W[j], self.S[j], self.N, self.K, out=C)
+        elif self.tc:
+            wqp.w8a16_gemm_tc(A, self.W[j], self.S[j], self.N, self.K, out=C)
+        else:
+            wqp.w8a16_gemm(A, self.W[j], self.S[j], self.N, self.K, out=C)
+
+    def free(self):
+        self.W = self.S = self.A = self.C = None
+
+
+def time_calls(fn, n, warm=20):
+    import torch
+
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / n   # us per call
+
+
+def sweep(l2, peak):
+    """us/call and GB/s for every workload (one line each), PDL on."""
+    import torch
+
+    import weight_only_quantized_packed_gb300 as wqp
+
+    out = []
+    specs = [
+        ("q2_gemv N=256 K=512", "q2", 256, 512, (1,), False, 0),
+        ("q2_gemv N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), False, 1),
+        ("w4a16_gemv N=5120 K=5120", "w4", 5120, 5120, tuple(range(1, 9)), False, 2),
+        ("w8a16_gemm N=17408 K=5120", "w8", 17408, 5120, (1, 4, 8, 16), False, 3),
+        ("w8a16_gemm N=5120 K=17408", "w8", 5120, 17408, (1, 4, 8, 16), False, 3),
+        ("w8a16_gemm_tc N=17408 K=5120", "w8", 17408, 5120, (1, 8, 16), True, 3),
+        ("w8a16_gemm_tc N=5120 K=17408", "w8", 5120, 17408, (1, 8, 16), True, 3),
+    ]
+    wqp.set_pdl(True)
+    try:
+        for name, fmt, N, K, Ms, tc, wl in specs:
+            w = Workload(fmt, N, K, Ms, l2, wl, tc=tc)
+            for M in Ms:
+                us = time_calls(lambda: w.call(M), max(50, min(2000, int(2e5 / max(1, w.wb // 4096)))))
+                gbs = w.wb / us / 1e3
+                out.append({"workload": name, "M": M, "us": round(us, 3), "gbs": round(gbs, 1),
+                            "pct_peak": round(100 * gbs / peak, 1)})
+            w.free()
+            torch.cuda.empty_cache()
+        # Decoder-layer sequence: qkv, o, gate+up, down, 8 layers cycled.
+        layer = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
+        ws = [Workload("q2", N, K, (1, 4, 8, 16), 0, 4, cap_bytes=0) for (N, K) in layer]
+        for w in ws:
+            w.nbuf = 8
+            w.W = [w.W[0]] + [w.W[0].clone() for _ in range(7)]
+        lb = sum(w.wb for w in ws)
+        for M in (1, 4, 8, 16):
+            us = time_calls(lambda: [w.call(M) for w in ws], 100)
+            out.append({"workload": "q2 decoder layer (qkv+o+gate_up+down), 8 layers cycled", "M": M,
+                        "us_per_layer": round(us, 3), "gbs": round(lb / us / 1e3, 1),
+                        "pct_peak": round(100 * lb / us / 1e3 / peak, 1)})
+        del ws
+        torch.cuda.empty_cache()
+    finally:
+        wqp.set_pdl(False)
+    return out
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import weight_only_quantized_packed_gb300 as wqp
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    peak, sm_max_nominal, peak_kind = peaks()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    H = HEADLINE
+    w = Workload(H["fmt"], H["N"], H["K"], H["Ms"], l2, 1)
+    bytes_step = w.wb * len(H["Ms"])
+    wqp.set_pdl(args.pdl)
+
+    def step():
+        for M in H["Ms"]:
+            w.call(M)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    stream = torch.cuda.current_stream()
+    with ClockSampler(dev) as clk:
+        # Keep the clock sampler's window filled with work before and after.
+        t_end = time.time() + 0.3
+        while time.time() < t_end:
+            step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+        if dist:
+            dist.barrier()
+        ms_total = e0.elapsed_time(e1)
+        # Per-kernel durations of the same launches (events around each call).
+        per = {M: [] for M in H["Ms"]}
+        n_inst = min(args.steps, 2000)
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in H["Ms"]] for _ in range(n_inst)]
+        for s in range(n_inst):
+            for (a, b), M in zip(ev[s], H["Ms"]):
+                a.record(stream)
+                w.call(M)
+                b.record(stream)
+        torch.cuda.synchronize()
+        for s in range(n_inst):
+            for (a, b), M in zip(ev[s], H["Ms"]):
+                per[M].append(a.elapsed_time(b) * 1e3)
+    wqp.set_pdl(False)
+    t = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * bytes_step * args.steps / (ms_total * 1e-3) / 1e9
+
+    # Dominant kernel: the call with the largest average duration.
+    avg = {M: statistics.fmean(v) for M, v in per.items()}
+    Mdom = max(avg, key=avg.get)
+    us_dom = avg[Mdom]
+    achieved = w.wb / (us_dom * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                "kernel": f"q2_gemv M={Mdom} N={H['N']} K={H['K']}",
+                "algorithmic_bytes_per_launch": w.wb,
+                "traffic": committed_traffic(f"q2_gemv_M{Mdom}_N{H['N']}_K{H['K']}")}
+    # ALU view of the same kernel: useful FMAs per second over the FP32 FMA peak.
+    sm_count = props.multi_processor_count
+    clk_sum = clk.summary()
+    f_mhz = clk_sum["sm_mhz"] or sm_max_nominal
+    fma_peak = sm_count * 128 * f_mhz * 1e6 / 1e12
+    roofline["alu_view"] = {"fma_tflops_achieved": round(Mdom * H["N"] * H["K"] / (us_dom * 1e-6) / 1e12, 3),
+                            "fma_tflops_peak": round(fma_peak, 2), "unit": "T FMA/s",
+                            "frac": round(Mdom * H["N"] * H["K"] / (us_dom * 1e-6) / 1e12 / fma_peak, 4),
+                            "peak_from": f"{sm_count} SMs x 128 FP32 lanes x {f_mhz:.0f} MHz"}
+
+    # End-to-end through the C ABI with host buffers (pinned): per step copy
+    # the three activation blocks in, compute, copy the three outputs back.
+    e2e = e2e_arm(w, H, max(20, min(args.steps, 2000)))
+    e2e["value"] = round(e2e["value"] * world, 2)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded; A ~ N(0,1) bf16, ternary codes U{0,1,2}, d U[0.01,0.05] fp16)",
+        "config": {"workload": "q2_gemv N=5120 K=5120, one step = M=1, 4, 8 calls",
+                   "weight_bytes_per_call": w.wb, "weight_buffers_cycled": w.nbuf,
+                   "l2": f"inputs larger than L2: {w.nbuf} weight buffers = {w.nbuf * w.wb / 2**20:.0f} MiB > 3x L2 ({l2 / 2**20:.0f} MiB)",
+                   "pdl": bool(args.pdl), "parallelism": f"replicas x{world}"},
+        "us_per_call": {str(M): round(avg[M], 3) for M in H["Ms"]},
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "roofline": roofline, "e2e": e2e,
+        "gpu_launches": args.steps * len(H["Ms"]),
+        "clocks": clk_sum,
+    }
+    w.free()
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_sweep:
+        line["sweep"] = sweep(l2, peak)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    return line
+
+
+def e2e_arm(w, H, steps):
+    import torch
+
+    import weight_only_quantized_packed_gb300 as wqp
+
+    hA = {M: w.A[M].cpu().pin_memory() for M in H["Ms"]}
+    hC = {M: torch.empty((M, w.N), dtype=torch.bfloat16).pin_memory() for M in H["Ms"]}
+    dA = {M: torch.empty_like(w.A[M]) for M in H["Ms"]}
+    h2d = sum(hA[M].numel() * 2 for M in H["Ms"])
+    d2h = sum(hC[M].numel() * 2 for M in H["Ms"])
+
+    def step():
+        for M in H["Ms"]:
+            dA[M].copy_(hA[M], non_blocking=True)
+            w.call(M, A=dA[M])
+            hC[M].copy_(w.C[M], non_blocking=True)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    wall = time.perf_counter() - t0
+    _ = wqp
+    return {"value": w.wb * len(H["Ms"]) * steps / (ms * 1e-3) / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "wall_s": round(wall, 4)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_baseline(seconds=10.0, rows=None):
+    """The CPU oracle, as it stands, timed on the host's cores on a bounded
+    sample of the headline step: the three calls restricted to the first
+    `rows` weight rows, repeated for about `seconds`."""
+    import oracle
+    from weight_only_quantized_packed_gb300 import synth
+
+    oracle.build()
+    H = HEADLINE
+    N, K = H["N"], H["K"]
+    rows = rows or N
+    W, _, _ = synth.q2_weights(N, K, synth.seed_for(1, 0))
+    W = W[:rows]
+    As = {M: synth.activations(M, K, synth.seed_for(1, M)) for M in H["Ms"]}
+    wb = synth.q2_weight_bytes(rows, K)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        for M in H["Ms"]:
+            oracle.q2_gemv(As[M], W, M, rows, K)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(wb * len(H["Ms"]) * n / dt / 1e9, 4), "unit": UNIT,
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} x (q2 M=1,4,8 over {rows} of {N} rows, K={K}); {dt:.1f} s"}
+
+
+def reference_arm(args, rank, world):
+    """The oracle as the reference arm: rank 0 only, on the host's cores."""
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.build()
+    H = HEADLINE
+    # Size each step so that warmup + steps finish in about a minute.
+    t_full = 0.7                          # s for a full step on 8 cores (measured)
+    per_step = 60.0 / max(1, args.steps + args.warmup)
+    rows = max(8, min(H["N"], int(H["N"] * per_step / t_full)))
+    from weight_only_quantized_packed_gb300 import synth
+
+    W, _, _ = synth.q2_weights(H["N"], H["K"], synth.seed_for(1, 0))
+    W = W[:rows]
+    As = {M: synth.activations(M, H["K"], synth.seed_for(1, M)) for M in H["Ms"]}
+    wb = synth.q2_weight_bytes(rows, H["K"])
+
+    def step():
+        for M in H["Ms"]:
+            oracle.q2_gemv(As[M], W, M, rows, H["K"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = wb * len(H["Ms"]) * args.steps / dt / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"q2_gemv N=5120 K=5120, one step = M=1, 4, 8 calls, sampled to {rows} rows"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": f"{rows} of {H['N']} rows per step"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="wqp", choices=["wqp", "reference"])
+    ap.add_argument("--pdl", type=int, default=1, help="programmatic dependent launch (1/0)")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", rank=rank, world_size=world)
+    line = gpu_arm(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

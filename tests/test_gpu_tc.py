@@ -1,0 +1,83 @@
+"""Parity of the tcgen05 swap-AB W8A16 GEMM with the CPU oracle (GPU needed).
+
+Tensor-core tolerance ("w8a16_gemm_m16.rs", module docs: within a few BF16
+ULP of the reference or under an absolute floor set by the reduction depth
+and the row's RMS): at most 4 BF16 ULP, or
+|gpu - oracle| < 1e-3 * sqrt(K) * rms(a[m,:]) * max_k |w[n,k]|, with w
+including its block scale. Exact-arithmetic inputs must match bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from tests import _gpu as G
+from tests._tol import bf16_to_f64, scalar_ok, tc_ok
+from weight_only_quantized_packed_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import weight_only_quantized_packed_gb300 as wqp
+
+    wqp.set_pdl(False)
+    yield
+    assert wqp.get_device_error() == 0
+
+
+def _check_tc(oracle_lib, d, C, what):
+    ref = G.run_oracle(oracle_lib, d)
+    a = synth.bf16_bits_to_f32(d["A"]).astype(np.float64)
+    a_rms = np.sqrt((a ** 2).mean(axis=1))
+    w_max = np.abs(oracle_lib.w8_dequant(d["W"], d["S"], d["N"], d["K"])).max(axis=1)
+    ok = tc_ok(C, ref, d["K"], a_rms, w_max)
+    bad = np.argwhere(~ok)
+    assert bad.size == 0, (what, len(bad), bad[:3], bf16_to_f64(C[tuple(bad[0])]),
+                           bf16_to_f64(ref.c[tuple(bad[0])]))
+    return scalar_ok(C, ref, d["K"])[0].mean()
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (200, 512), (1000, 1024), (384, 2048), (77, 640)])
+def test_tc_parity_small(oracle_lib, N, K):
+    for M in (1, 5, 16):
+        d = G.make("w8", M, N, K, seed=300 + N + K + M)
+        C = G.host_bits(G.run_gpu(d, tc=True))
+        _check_tc(oracle_lib, d, C, f"M={M} N={N} K={K}")
+
+
+def test_tc_exact_arithmetic_bit_exact(oracle_lib):
+    r = np.random.default_rng(5)
+    M, N, K = 16, 300, 2048
+    a = r.integers(-4, 5, size=(M, K)).astype(np.float32)
+    A = synth.bf16_bits_from_f32(a)
+    W = synth.e4m3_round(r.integers(-16, 17, size=(N, K)) / 8.0)
+    S = (2.0 ** r.integers(-2, 3, size=((N + 127) // 128, K // 128))).astype(np.float32)
+    d = {"A": A, "dA": G.dev_bf16(A), "M": M, "N": N, "K": K, "fmt": "w8", "W": W, "S": S,
+         "dW": G.dev_u8(W), "dS": G.dev_f32(S)}
+    C = G.host_bits(G.run_gpu(d, tc=True))
+    assert np.array_equal(C, G.run_oracle(oracle_lib, d).c)
+
+
+def test_tc_split_k_deterministic_and_row_independent():
+    """N = 640 splits K over a cluster; repeated calls give identical bits and
+    each row does not depend on the other activation rows."""
+    d = G.make("w8", 16, 640, 5120, seed=11)
+    c1 = G.host_bits(G.run_gpu(d, tc=True))
+    c2 = G.host_bits(G.run_gpu(d, tc=True))
+    assert np.array_equal(c1, c2)
+    one = G.host_bits(G.run_gpu(d, tc=True, A=d["dA"][3:4]))
+    assert np.array_equal(one[0], c1[3])
+
+
+@pytest.mark.parametrize("N,K,Ms", [(17408, 5120, (16, 1)), (5120, 17408, (16, 8))])
+def test_tc_full_size(oracle_lib, N, K, Ms):
+    for M in Ms:
+        d = G.make("w8", M, N, K, seed=synth.seed_for(3, M))
+        C = G.host_bits(G.run_gpu(d, tc=True))
+        frac = _check_tc(oracle_lib, d, C, f"full M={M} N={N} K={K}")
+        assert frac > 0.99   # almost every output is also within the scalar 1-ULP term

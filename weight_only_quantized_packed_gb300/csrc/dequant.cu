@@ -13,15 +13,16 @@ __global__ void q2_dequant_kernel(const uint8_t* W, float* out, int N, int K) {
     const long long blk = i >> 3;
     const int w = static_cast<int>(i & 7);
     const uint8_t* b = W + blk * 34;
-    uint32_t p[8];
+    float2 v[8];
     const uint16_t* b16 = reinterpret_cast<const uint16_t*>(b);
-    q2_decode_word(static_cast<uint32_t>(__ldg(b16 + 2 * w)) | (static_cast<uint32_t>(__ldg(b16 + 2 * w + 1)) << 16), p);
+    q2_decode_f32(static_cast<uint32_t>(__ldg(b16 + 2 * w)) | (static_cast<uint32_t>(__ldg(b16 + 2 * w + 1)) << 16), v);
     const float d = __half2float(__ushort_as_half(__ldg(b16 + 16)));
     float* o = out + (blk / G) * static_cast<long long>(K) + (blk % G) * 128 + 16 * w;
+    // (c - 1) * 4^j * 4^-j is exact; then one multiply by d, as in the oracle.
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      o[j] = bf16lo(p[j]) * d;
-      o[j + 8] = bf16hi(p[j]) * d;
+    for (int i = 0; i < 8; ++i) {
+      o[2 * i] = (v[i].x * (1.0f / q2_pos_weight(2 * i))) * d;
+      o[2 * i + 1] = (v[i].y * (1.0f / q2_pos_weight(2 * i + 1))) * d;
     }
   }
 }

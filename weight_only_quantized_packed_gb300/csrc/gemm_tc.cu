@@ -1,5 +1,381 @@
-// Placeholder until the tcgen05 swap-AB kernel lands.
-#include "internal.h"
+// Tensor-core (tcgen05) swap-AB decode GEMM for FP8 E4M3 weights with FP32
+// 128x128 block scales, 1 <= M <= 16
+// ("metrale_model_layers/layers/ops/w8a16_gemm_m16.rs": doc of
+// `w8a16_gemm_m16` for the operands and the 16-row M tile; module docs for
+// the block scale being folded once per 128-K block onto an FP32 outer
+// accumulator, never per element and never into BF16).
+//
+// Swap-AB: the 128 weight rows of a tile are the MMA's M side and the M <= 16
+// activation rows, zero-padded to 16, are its N side:
+//   D[n, m] = sum_k W[n, k] * A[m, k]     (tcgen05.mma kind::f16, M=128 N=16 K=16)
+// E4M3 values are exactly representable in BF16, so the products are exact.
+// The tensor core reduces each 16-K step in its own order, so the result is
+// not bit-identical to the scalar kernel.
+//
+// One CTA = one 128-row tile x a contiguous range of 128-K groups. Roles:
+//   warp 8      TMA: raw FP8 tiles [128 rows x 128 B] (128-byte swizzle) and
+//               activation tiles [16 rows x 64 K] x 2 (128-byte swizzle, rows
+//               past M are zero-filled), through mbarrier rings;
+//   warps 0..7  convert FP8 -> BF16 into the K-major, no-swizzle operand tile
+//               (8x16-byte core matrices), one row and half a group per thread;
+//   warp 9      allocates TMEM and issues the 8 MMAs of each group into its
+//               own 16-column accumulator slot, then commits;
+//   warps 0..3  also fold each group: tcgen05.ld of the slot (lane = weight
+//               row, column = activation row), acc[m] += s * D[m] in FP32.
+// When N is small, K is split over a thread-block cluster of up to 8 CTAs.
+// The partial sums are added in rank order through distributed shared memory
+// (deterministic, no global scratch).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "decode.cuh"
+#include "tc.cuh"
+
 namespace wqp {
-cudaError_t launch_w8a16_gemm_tc(const GemvArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace tc {
+
+constexpr int BM = 128;            // weight rows per tile (MMA M)
+constexpr int BN = 16;             // activation rows (MMA N)
+constexpr int GK = 128;            // K per group = block-scale granularity
+constexpr int kConvWarps = 8;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int SR = 6;              // raw stages (96 KB of weights in flight)
+constexpr int SA = 4;              // activation stages
+constexpr int SO = 2;              // operand stages
+constexpr int NACC = 4;            // TMEM accumulator slots
+constexpr int LAG = NACC - 1;      // fold group j - LAG after converting group j
+constexpr uint32_t kTmemCols = 64; // NACC * 16, rounded to a power of two >= 32
+
+constexpr int kOpBytes = BM * GK * 2;      // 32 KB
+constexpr int kRawBytes = BM * GK;         // 16 KB (FP8)
+constexpr int kActBytes = BN * GK * 2;     // 4 KB
+constexpr int kOpOff = 0;
+constexpr int kRawOff = kOpOff + SO * kOpBytes;
+constexpr int kActOff = kRawOff + SR * kRawBytes;
+constexpr int kSmemBytes = kActOff + SA * kActBytes;
+constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack for 1024-byte alignment
+static_assert(BM * BN * 4 <= SR * kRawBytes, "split-K partials alias the raw ring");
+
+struct TcParams {
+  const float* scales;     // [ceil(N/128), K/128]
+  uint16_t* C;
+  int M, N, K, ldc;
+  int splits;              // CTAs per tile (cluster size)
+  unsigned* err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    w8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                 TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t raw_full[SR], raw_empty[SR];
+  __shared__ __align__(8) uint64_t act_full[SA], act_empty[SA];
+  __shared__ __align__(8) uint64_t op_full[SO], op_empty[SO];
+  __shared__ __align__(8) uint64_t acc_full[NACC], acc_empty[NACC];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int splits = p.splits;
+  const int tile = blockIdx.x / splits;
+  const int rank = blockIdx.x - tile * splits;      // == %cluster_ctarank
+  const int n0 = tile * BM;
+  const int G = p.K / GK;
+  const int g_begin = (rank * G) / splits;
+  const int g_end = ((rank + 1) * G) / splits;
+  const int ng = g_end - g_begin;
+  volatile int* abort_flag = &abort_sh;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SR; ++i) { mbar_init(smem_u32(&raw_full[i]), 1); mbar_init(smem_u32(&raw_empty[i]), kConvWarps); }
+    for (int i = 0; i < SA; ++i) { mbar_init(smem_u32(&act_full[i]), 1); mbar_init(smem_u32(&act_empty[i]), 1); }
+    for (int i = 0; i < SO; ++i) { mbar_init(smem_u32(&op_full[i]), kConvWarps); mbar_init(smem_u32(&op_empty[i]), 1); }
+    for (int i = 0; i < NACC; ++i) { mbar_init(smem_u32(&acc_full[i]), 1); mbar_init(smem_u32(&acc_empty[i]), 4); }
+    abort_sh = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmA);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_launch_dependents();
+  const uint32_t tmem = tmem_base_sh;
+
+  float acc[BN];
+#pragma unroll
+  for (int m = 0; m < BN; ++m) acc[m] = 0.0f;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ TMA
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int raw_issued = 0, act_issued = 0;
+      bool ok = true;
+      for (int j = 0; j < ng && j < SR; ++j) {
+        mbar_arrive_expect_tx(smem_u32(&raw_full[j]), kRawBytes);
+        tma_load_2d_hint(sbase + kRawOff + j * kRawBytes, &tmW, (g_begin + j) * GK, n0,
+                         smem_u32(&raw_full[j]), pol);
+        raw_issued = j + 1;
+      }
+      pdl_wait();                          // activations may come from the previous kernel
+      for (int j = 0; j < ng && ok; ++j) {
+        const int sa = j % SA;
+        if (j >= SA && !(ok = wait_or_abort(smem_u32(&act_empty[sa]), ((j / SA) - 1) & 1, p.err, abort_flag))) break;
+        mbar_arrive_expect_tx(smem_u32(&act_full[sa]), kActBytes);
+        const uint32_t dst = sbase + kActOff + sa * kActBytes;
+        tma_load_2d(dst, &tmA, (g_begin + j) * GK, 0, smem_u32(&act_full[sa]));
+        tma_load_2d(dst + kActBytes / 2, &tmA, (g_begin + j) * GK + 64, 0, smem_u32(&act_full[sa]));
+        act_issued = j + 1;
+        const int jn = j + SR;
+        if (jn < ng) {
+          const int sr = jn % SR;
+          if (!(ok = wait_or_abort(smem_u32(&raw_empty[sr]), ((jn / SR) - 1) & 1, p.err, abort_flag))) break;
+          mbar_arrive_expect_tx(smem_u32(&raw_full[sr]), kRawBytes);
+          tma_load_2d_hint(sbase + kRawOff + sr * kRawBytes, &tmW, (g_begin + jn) * GK, n0,
+                           smem_u32(&raw_full[sr]), pol);
+          raw_issued = jn + 1;
+        }
+      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      for (int j = max(0, raw_issued - SR); j < raw_issued; ++j)
+        mbar_wait(smem_u32(&raw_full[j % SR]), (j / SR) & 1, p.err);
+      for (int j = max(0, act_issued - SA); j < act_issued; ++j)
+        mbar_wait(smem_u32(&act_full[j % SA]), (j / SA) & 1, p.err);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      int issued = 0;
+      for (int j = 0; j < ng; ++j) {
+        const int so = j % SO, sa = j % SA, sc = j % NACC;
+        if (!wait_or_abort(smem_u32(&op_full[so]), (j / SO) & 1, p.err, abort_flag)) break;
+        if (!wait_or_abort(smem_u32(&act_full[sa]), (j / SA) & 1, p.err, abort_flag)) break;
+        if (j >= NACC && !wait_or_abort(smem_u32(&acc_empty[sc]), ((j / NACC) - 1) & 1, p.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t opb = sbase + kOpOff + so * kOpBytes;
+        const uint32_t actb = sbase + kActOff + sa * kActBytes;
+#pragma unroll
+        for (int i = 0; i < GK / 16; ++i) {
+          // Operand: core matrix (k8, r8) at (k8 * 16 + r8) * 128 B; one MMA
+          // covers k8 = 2i, 2i+1: LBO (K step) = 2048 B, SBO (8-row step) = 128 B.
+          const uint64_t ad = sdesc(opb + i * 4096, 2048, 128, 0);
+          // Activations: 128-byte swizzled rows of 64 K; 32 B per 16-K step,
+          // the second 64 K in the second box; SBO = 1024 B (8-row atoms).
+          const uint64_t bd = sdesc(actb + (i >> 2) * (kActBytes / 2) + (i & 3) * 32, 16, 1024, 2);
+          mma_bf16(tmem + sc * 16, ad, bd, idesc, i > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&op_empty[so]));
+        mma_commit(smem_u32(&act_empty[sa]));
+        mma_commit(smem_u32(&acc_full[sc]));
+        issued = j + 1;
+      }
+      // Drain: all MMAs done before TMEM is freed.
+      if (issued > 0) {
+        const int j = issued - 1;
+        mbar_wait(smem_u32(&acc_full[j % NACC]), (j / NACC) & 1, p.err);
+      }
+    }
+  } else {
+    // ------------------------------------------------------ convert (+ fold)
+    const int q = warp & 3;                 // TMEM lane quarter / row block
+    const int h = warp >> 2;                // which 64-K half of a group
+    const int r = q * 32 + lane;            // row within the tile
+    const bool folds = warp < 4;
+    const float* srow = p.scales + static_cast<size_t>(tile) * G;   // 128-row tiles == scale rows
+    int folded = 0;
+    auto fold = [&](int j) -> bool {
+      const int sc = j % NACC;
+      // Warp-uniform outcome: tcgen05.ld below is .sync.aligned.
+      const bool got = wait_or_abort(smem_u32(&acc_full[sc]), (j / NACC) & 1, p.err, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, got)) return false;
+      tc_fence_after();
+      float v[16];
+      tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + sc * 16, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[sc]));
+      const float s = __ldg(srow + g_begin + j);
+#pragma unroll
+      for (int m = 0; m < BN; ++m) acc[m] = fmaf(v[m], s, acc[m]);
+      return true;
+    };
+    bool ok = true;
+    for (int j = 0; j < ng && ok; ++j) {
+      const int sr = j % SR, so = j % SO;
+      const bool g1 = wait_or_abort(smem_u32(&raw_full[sr]), (j / SR) & 1, p.err, abort_flag);
+      const bool g2 = g1 && (j < SO || wait_or_abort(smem_u32(&op_empty[so]), ((j / SO) - 1) & 1, p.err, abort_flag));
+      if (!__all_sync(0xFFFFFFFFu, g1 && g2)) { ok = false; break; }
+      const uint8_t* raw = smem + kRawOff + sr * kRawBytes + r * 128;
+      uint8_t* op = smem + kOpOff + so * kOpBytes + (r >> 3) * 128 + (r & 7) * 16;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int c = h * 4 + c4;                                   // 16-byte chunk = 16 K
+        const uint4 v = *reinterpret_cast<const uint4*>(raw + ((c ^ (r & 7)) << 4));
+        uint4 lo, hi;
+        e4m3x4_to_bf16(v.x, lo.x, lo.y);
+        e4m3x4_to_bf16(v.y, lo.z, lo.w);
+        e4m3x4_to_bf16(v.z, hi.x, hi.y);
+        e4m3x4_to_bf16(v.w, hi.z, hi.w);
+        *reinterpret_cast<uint4*>(op + (2 * c) * 2048) = lo;        // core matrix k8 = 2c
+        *reinterpret_cast<uint4*>(op + (2 * c + 1) * 2048) = hi;    // k8 = 2c + 1
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&op_full[so]));
+        mbar_arrive(smem_u32(&raw_empty[sr]));
+      }
+      if (folds && j >= LAG) {
+        if (!fold(j - LAG)) { ok = false; break; }
+        folded = j - LAG + 1;
+      }
+    }
+    if (folds && ok)
+      for (int j = folded; j < ng; ++j)
+        if (!fold(j)) { ok = false; break; }
+  }
+
+  // ---------------------------------------------------------- reduce + store
+  __syncthreads();
+  const bool failed = *abort_flag != 0;
+  float* red = reinterpret_cast<float*>(smem + kRawOff);   // raw ring is idle now
+  if (splits > 1) {
+    if (warp < 4 && rank != 0) {
+      float4* dst = reinterpret_cast<float4*>(red + (warp * 32 + lane) * BN);
+#pragma unroll
+      for (int i = 0; i < BN / 4; ++i) dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+    }
+    cluster_sync();
+    if (warp < 4 && rank == 0) {
+      const uint32_t mine = smem_u32(red + (warp * 32 + lane) * BN);
+      for (int q = 1; q < splits; ++q) {
+        const uint32_t rem = mapa_shared(mine, q);
+#pragma unroll
+        for (int i = 0; i < BN / 4; ++i) {
+          const float4 v = ld_dsmem_f4(rem + 16 * i);
+          acc[4 * i] += v.x;
+          acc[4 * i + 1] += v.y;
+          acc[4 * i + 2] += v.z;
+          acc[4 * i + 3] += v.w;
+        }
+      }
+    }
+    cluster_sync();                       // remote partials stay alive until read
+  }
+  if (warp < 4 && rank == 0 && !failed) {
+    const int n = n0 + warp * 32 + lane;
+    if (n < p.N)
+      for (int m = 0; m < p.M; ++m) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc[m]);
+  }
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int choose_splits(int tiles, int groups, int num_sms) {
+  int s = num_sms / tiles;                   // one CTA per SM, a single wave
+  if (s < 1) s = 1;
+  if (s > 8) s = 8;                          // portable cluster size
+  if (s > groups) s = groups;
+  return s;
+}
+
+}  // namespace tc
+
+cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mw, ma;
+  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, static_cast<uint64_t>(a.K),
+                              static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K), GK, BM,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  e = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, static_cast<uint64_t>(a.K),
+                  static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda) * 2, 64, BN,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(w8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = (a.N + BM - 1) / BM;
+  const int G = a.K / GK;
+  TcParams p;
+  p.scales = static_cast<const float*>(a.scales);
+  p.C = static_cast<uint16_t*>(a.C);
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.ldc = a.ldc;
+  p.splits = choose_splits(tiles, G, a.num_sms);
+  p.err = a.err;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles * p.splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = p.splits;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (a.pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, w8_tc_kernel, mw, ma, p);
+}
+
 }  // namespace wqp

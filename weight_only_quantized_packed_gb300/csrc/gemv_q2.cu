@@ -6,13 +6,12 @@
 namespace wqp {
 
 struct Q2Fmt {
-  // One ring stage holds 8 groups (1024 K) of a row: 8 blocks x 34 bytes.
-  static constexpr int kWBytesPerRow = 8 * 34;
-  static constexpr bool kJ8 = true;
+  static constexpr int kTK = 1024;                 // 8 groups per stage
+  static constexpr int kWRow = 8 * 34;             // 8 blocks x 34 bytes
   // Row tiles start at byte 34 * (n * K/128 + 8 t); 16-byte aligned for every
   // n iff K/128 is a multiple of 8.
   static bool bulk_ok(int K) { return (K / 128) % 8 == 0; }
-  __device__ static uint32_t row_tile_bytes(int, int, int tg) { return 34u * tg; }
+  __device__ static uint32_t row_tile_bytes(int tg) { return 34u * tg; }
   __device__ static void issue_row_bulk(const ScalarParams& p, int n, int t, int tg, uint32_t dst,
                                         uint32_t bar, uint64_t pol) {
     const size_t G = static_cast<size_t>(p.K >> 7);
@@ -25,10 +24,13 @@ struct Q2Fmt {
     uint16_t* d = reinterpret_cast<uint16_t*>(dst);
     for (int i = lane; i < 17 * tg; i += 32) d[i] = __ldg(src + i);
   }
+  // The activation at position p of a 16-K segment is pre-scaled by the
+  // inverse of the decoded weight's position factor (see q2_decode_f32).
+  __device__ static constexpr float prescale(int pos) { return 1.0f / q2_pos_weight(pos); }
   // Segment sg of a tile = word (sg % 8) of block (sg / 8): K offset 16 * sg.
   __device__ static void decode(const ScalarParams&, int, int, int sg, const uint8_t* sW, Seg& g) {
     const uint8_t* blk = sW + (sg >> 3) * 34;
-    q2_decode_word(q2_code_word(blk, sg & 7), g.p);
+    q2_decode_f32(q2_code_word(blk, sg & 7), g.w);
     g.s = q2_scale(blk);
   }
 };

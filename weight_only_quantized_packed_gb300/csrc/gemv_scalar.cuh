@@ -2,123 +2,40 @@
 // format, with exact-M specialisation (M = 1..16, one template instance per M).
 //
 // Thread map (after "spark_model/layers/ops/gemv_q2_vec.rs", doc of
-// `q2_0_gemv_vec`: one warp per output row, eight rows per CTA):
-//   warps 0..7  consumers: warp w owns output row n0 + w and keeps M FP32
-//               accumulators, so every weight word is read once for all M rows
-//               (doc of `q2_0_gemv_vec_batchm`);
-//   warp 8      producer: one lane streams the CTA's 8-row weight slab and
-//               the M activation rows through a STAGES-deep shared-memory ring
-//               of K tiles with non-multicast bulk copies (cp.async.bulk) and
-//               mbarriers. Odd shapes whose rows are not 16-byte aligned use
-//               plain loads by the whole producer warp instead.
+// `q2_0_gemv_vec`, and the register-tiled T=2 tier of
+// "spark_model/layers/w4a16_gemv_tiers.rs", doc of `resolve`):
+//   warps 0..7  consumers: warp w owns output rows n0 + 2w and n0 + 2w + 1
+//               and keeps M FP32 accumulator pairs per row, so every weight
+//               word is read once for all M rows (doc of
+//               `q2_0_gemv_vec_batchm`) and every activation load serves two
+//               weight rows;
+//   warp 8      producer: one lane streams the CTA's 16-row weight slab and
+//               the M BF16 activation rows through a STAGES-deep ring of K
+//               tiles with non-multicast bulk copies (cp.async.bulk) and
+//               mbarriers. If the rows are not 16-byte aligned, the whole
+//               producer warp copies with plain loads instead.
+// Per K tile the consumers first widen the activation tile to FP32 in shared
+// memory (double-buffered, one named barrier per tile), then stream the
+// weight segments.
 //
 // Per-row arithmetic (identical for every M, so a batched row equals the M = 1
-// row bit for bit): for each 16-weight segment a lane owns, two FP32 chains
-// (k = 0..7 and k = 8..15 of the segment) of fma(a_bf16, w_bf16) are added,
-// the segment's scale is folded with one FP32 fma onto the lane accumulator,
-// and the 32 lanes are summed by a fixed xor-butterfly. The order of the
-// segments, of the K tiles and of the butterfly depends only on N and K.
-// Weights are converted exactly to BF16 (every Q2_0/E2M1/E4M3 value is a BF16
-// value), activations stay BF16, and fma.rn.f32.bf16 forms the exact product
-// with a single FP32 rounding of the sum.
+// row bit for bit): weights are decoded to exact FP32 values. For each
+// 16-weight segment a lane owns, two chains of packed FFMA2 (k = 0..7 and
+// k = 8..15, even and odd k in the two halves) are added, the segment's scale
+// is folded with one FFMA2 onto the lane's accumulator pair, and at the end
+// the pair is summed and the 32 lanes reduced by a fixed xor-butterfly. The
+// order depends only on N and K, never on M.
 #pragma once
 #include "common.cuh"
 
 namespace wqp {
 
-constexpr int kRows = 8;             // output rows per CTA (one consumer warp each)
-constexpr int kConsumers = kRows * 32;
-constexpr int kThreads = kConsumers + 32;
-constexpr int kTileK = 1024;         // K elements per ring stage
-constexpr int kSegsPerTile = kTileK / 16;
+constexpr int kWarpsC = 8;                  // consumer warps
+constexpr int kRowsPerWarp = 2;
+constexpr int kRows = kWarpsC * kRowsPerWarp;  // output rows per CTA
+constexpr int kThreads = (kWarpsC + 1) * 32;
 
-// fma.rn.f32.bf16 with explicit operand halves: fma_XY(a2, b2, c) =
-// a2.X * b2.Y + c, X/Y in {l, h} (low / high BF16 of the 32-bit register).
-__device__ __forceinline__ float fma_ll(uint32_t a2, uint32_t b2, float c) {
-  float d;
-  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
-      : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float fma_hh(uint32_t a2, uint32_t b2, float c) {
-  float d;
-  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
-      : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float fma_lh(uint32_t a2, uint32_t b2, float c) {
-  float d;
-  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, al, bh, %3;\n\t}"
-      : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float fma_hl(uint32_t a2, uint32_t b2, float c) {
-  float d;
-  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, ah, bl, %3;\n\t}"
-      : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
-  return d;
-}
-
-// A segment of 16 consecutive weights w[0..15] decoded to BF16 pairs, plus
-// the segment's scale. Natural layout: p[i] = (lo: w[2i], hi: w[2i+1]).
-// J8 layout (Q2_0 decode): p[j] = (lo: w[j], hi: w[j+8]).
-struct Seg {
-  uint32_t p[8];
-  float s;
-};
-
-// Dot products of one decoded segment with the M activation rows' matching
-// 16 BF16 values (a[m][0..15] at sA + m * lda_s), folded onto acc[m]. Chain
-// c0 runs over k = 0..7 and c1 over k = 8..15, both in ascending k.
-template <int M, bool J8>
-__device__ __forceinline__ void seg_fma(const Seg& g, const uint16_t* sA, int lda_s, float* acc) {
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const uint4 a0 = *reinterpret_cast<const uint4*>(sA + m * lda_s);
-    const uint4 a1 = *reinterpret_cast<const uint4*>(sA + m * lda_s + 8);
-    float c0 = 0.0f, c1 = 0.0f;
-    if (!J8) {
-      c0 = fma_ll(a0.x, g.p[0], c0);
-      c0 = fma_hh(a0.x, g.p[0], c0);
-      c0 = fma_ll(a0.y, g.p[1], c0);
-      c0 = fma_hh(a0.y, g.p[1], c0);
-      c0 = fma_ll(a0.z, g.p[2], c0);
-      c0 = fma_hh(a0.z, g.p[2], c0);
-      c0 = fma_ll(a0.w, g.p[3], c0);
-      c0 = fma_hh(a0.w, g.p[3], c0);
-      c1 = fma_ll(a1.x, g.p[4], c1);
-      c1 = fma_hh(a1.x, g.p[4], c1);
-      c1 = fma_ll(a1.y, g.p[5], c1);
-      c1 = fma_hh(a1.y, g.p[5], c1);
-      c1 = fma_ll(a1.z, g.p[6], c1);
-      c1 = fma_hh(a1.z, g.p[6], c1);
-      c1 = fma_ll(a1.w, g.p[7], c1);
-      c1 = fma_hh(a1.w, g.p[7], c1);
-    } else {
-      c0 = fma_ll(a0.x, g.p[0], c0);
-      c0 = fma_hl(a0.x, g.p[1], c0);
-      c0 = fma_ll(a0.y, g.p[2], c0);
-      c0 = fma_hl(a0.y, g.p[3], c0);
-      c0 = fma_ll(a0.z, g.p[4], c0);
-      c0 = fma_hl(a0.z, g.p[5], c0);
-      c0 = fma_ll(a0.w, g.p[6], c0);
-      c0 = fma_hl(a0.w, g.p[7], c0);
-      c1 = fma_lh(a1.x, g.p[0], c1);
-      c1 = fma_hh(a1.x, g.p[1], c1);
-      c1 = fma_lh(a1.y, g.p[2], c1);
-      c1 = fma_hh(a1.y, g.p[3], c1);
-      c1 = fma_lh(a1.z, g.p[4], c1);
-      c1 = fma_hh(a1.z, g.p[5], c1);
-      c1 = fma_lh(a1.w, g.p[6], c1);
-      c1 = fma_hh(a1.w, g.p[7], c1);
-    }
-    acc[m] = fmaf(c0 + c1, g.s, acc[m]);
-  }
-}
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
 
 // Kernel parameters (passed by value).
 struct ScalarParams {
@@ -131,20 +48,42 @@ struct ScalarParams {
   unsigned* err;
 };
 
-// Format traits interface (see gemv_q2.cu, gemv_w4.cu, gemv_w8.cu):
-//   static constexpr int kWBytesPerRow;          // bytes of one row's full K tile in smem
-//   static bool bulk_ok(int K);                  // host: bulk-copy fast path allowed
-//   __device__ static uint32_t row_tile_bytes(int K, int tile, int segs);   // bytes copied per row
-//   __device__ static void issue_row_bulk(...)   // producer lane: bulk copy one row's tile
-//   __device__ static void copy_row_plain(...)   // producer warp: plain-load copy
-//   __device__ static void decode(...)           // consumer: one segment -> Seg
+// A decoded 16-weight segment: w[i] = (w_{2i}, w_{2i+1}) as FP32, plus scale.
+struct Seg {
+  float2 w[8];
+  float s;
+};
+
+// Position of the 16-byte chunk j (0..3) of segment sg in the FP32 activation
+// buffer: XOR-swizzled so that the 8 lanes of a shared-memory phase, which
+// read 8 consecutive segments, hit 8 distinct bank groups.
+__device__ __forceinline__ int fa_chunk(int sg, int j) { return sg * 4 + (j ^ ((sg >> 1) & 3)); }
+
+// Format traits interface (gemv_q2.cu, gemv_w4.cu, gemv_w8.cu):
+//   kTK                 K elements per ring stage (multiple of 128)
+//   kWRow               weight bytes of one row per stage
+//   bulk_ok(K)          host: bulk-copy fast path allowed for this K
+//   row_tile_bytes(tg)  bytes of one row's tile with tg groups
+//   issue_row_bulk(...) producer lane: bulk copies of one row's tile
+//   copy_row_plain(...) producer warp: plain-load copy of one row's tile
+//   prescale(p)         factor applied to a[k] when widened (p = k % 16)
+//   decode(...)         consumer: one segment of one row -> Seg
+template <class F, int M>
+struct ScalarCfg {
+  static constexpr int kStages = (M <= 4) ? 6 : (M <= 8 ? 4 : 2);
+  static constexpr int kWStage = kRows * F::kWRow;
+  static constexpr int kAStage = M * F::kTK * 2;
+  static constexpr int kStageBytes = ((kWStage + kAStage) + 127) / 128 * 128;
+  static constexpr int kFABytes = M * F::kTK * 4;           // one FP32 activation buffer
+  static constexpr int kSmem = kStages * kStageBytes + 2 * kFABytes;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
 
 template <class F, int M, bool BULK>
 __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
-  constexpr int kStages = (M <= 4) ? 6 : (M <= 8 ? 4 : 3);
-  constexpr int kWStage = kRows * F::kWBytesPerRow;                  // weight bytes per stage
-  constexpr int kAStage = M * kTileK * 2;                           // activation bytes per stage
-  constexpr int kStageBytes = ((kWStage + kAStage) + 127) / 128 * 128;
+  using Cfg = ScalarCfg<F, M>;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int TK = F::kTK;
 
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -155,51 +94,52 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
   const int n0 = blockIdx.x * kRows;
   const int rows = min(kRows, p.N - n0);
   const int K = p.K;
-  const int G = K >> 7;                                   // 128-wide groups per row
-  const int tiles = (K + kTileK - 1) / kTileK;
+  const int G = K >> 7;                          // 128-wide groups per row
+  constexpr int kGT = TK / 128;                  // groups per full tile
+  const int tiles = (G + kGT - 1) / kGT;
+  float* fA = reinterpret_cast<float*>(smem + kStages * Cfg::kStageBytes);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), kRows);
+      mbar_init(smem_u32(&empty_bar[s]), kWarpsC);
     }
     mbar_fence_init();
   }
   __syncthreads();
   pdl_launch_dependents();
 
-  if (warp == kRows) {
+  if (warp == kWarpsC) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
     int issued = 0;
-    bool ok = true;
-    for (int t = 0; t < tiles && ok; ++t) {
+    for (int t = 0; t < tiles; ++t) {
       const int s = t % kStages;
       if (t >= kStages) {
         uint32_t done = 0;
         if (lane == 0) done = mbar_wait(smem_u32(&empty_bar[s]), ((t / kStages) - 1) & 1, p.err);
         done = __shfl_sync(0xFFFFFFFFu, done, 0);
-        if (!done) { ok = false; break; }
+        if (!done) break;
       }
-      const int tg = min(8, G - t * 8);                    // groups in this tile
-      uint8_t* sW = smem + s * kStageBytes;
-      uint8_t* sAs = sW + kWStage;
-      const uint32_t wrow = F::row_tile_bytes(K, t, tg);
+      const int tg = min(kGT, G - t * kGT);      // groups in this tile
+      uint8_t* sW = smem + s * Cfg::kStageBytes;
+      uint8_t* sAs = sW + Cfg::kWStage;
       const uint32_t abytes = static_cast<uint32_t>(tg) * 128 * 2;
       const uint32_t fb = smem_u32(&full_bar[s]);
       if (!BULK) {
-        for (int r = 0; r < rows; ++r) F::copy_row_plain(p, n0 + r, t, tg, sW + r * F::kWBytesPerRow, lane);
+        for (int r = 0; r < rows; ++r) F::copy_row_plain(p, n0 + r, t, tg, sW + r * F::kWRow, lane);
         __threadfence_block();
         __syncwarp();
       }
       if (lane == 0) {
-        const uint32_t tx = (BULK ? wrow * rows : 0u) + abytes * M;
+        const uint32_t tx = (BULK ? F::row_tile_bytes(tg) * rows : 0u) + abytes * M;
         mbar_arrive_expect_tx(fb, tx);
         if (BULK)
-          for (int r = 0; r < rows; ++r) F::issue_row_bulk(p, n0 + r, t, tg, smem_u32(sW + r * F::kWBytesPerRow), fb, pol);
+          for (int r = 0; r < rows; ++r)
+            F::issue_row_bulk(p, n0 + r, t, tg, smem_u32(sW + r * F::kWRow), fb, pol);
         if (t == 0) pdl_wait();            // activations may come from the previous kernel
         for (int m = 0; m < M; ++m)
-          bulk_g2s(smem_u32(sAs + m * kTileK * 2), p.A + static_cast<size_t>(m) * p.lda + t * kTileK, abytes, fb);
+          bulk_g2s(smem_u32(sAs + m * TK * 2), p.A + static_cast<size_t>(m) * p.lda + t * TK, abytes, fb);
       }
       issued = t + 1;
     }
@@ -211,52 +151,105 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
   }
 
   // -------------------------------------------------------------- consumers
-  float acc[M];
+  float2 acc[kRowsPerWarp][M];
 #pragma unroll
-  for (int m = 0; m < M; ++m) acc[m] = 0.0f;
-  const bool live = warp < rows;
-  const int n = n0 + warp;
+  for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
+  const int r0 = warp * kRowsPerWarp;             // first local row of this warp
   bool ok = true;
   for (int t = 0; t < tiles; ++t) {
     const int s = t % kStages;
-    // Every lane waits (acquire), and the warp agrees on the outcome, so a
-    // timeout never splits the warp before the __syncwarp below.
-    const bool got = mbar_wait(smem_u32(&full_bar[s]), (t / kStages) & 1, p.err);
-    if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
-    const int tg = min(8, G - t * 8);
+    // Every lane waits (acquire) and the warp agrees on the outcome, so a
+    // timeout never splits the warp. After a timeout the loop keeps running
+    // the named barrier (no compute) so the other consumer warps never wait
+    // on it for ever.
+    if (ok) {
+      const bool got = mbar_wait(smem_u32(&full_bar[s]), (t / kStages) & 1, p.err);
+      if (!__all_sync(0xFFFFFFFFu, got)) ok = false;
+    }
+    const int tg = min(kGT, G - t * kGT);
     const int segs = tg * 8;
-    const uint8_t* sW = smem + s * kStageBytes + warp * F::kWBytesPerRow;
-    const uint16_t* sAs = reinterpret_cast<const uint16_t*>(smem + s * kStageBytes + kWStage);
-    if (live) {
+    const uint8_t* sW = smem + s * Cfg::kStageBytes;
+    const uint16_t* sAs = reinterpret_cast<const uint16_t*>(sW + Cfg::kWStage);
+    float* fAt = fA + (t & 1) * (M * TK);
+    // Widen the activation tile to FP32, one 16-element segment per unit,
+    // applying the format's per-position pre-scale (a power of two).
+    if (ok) {
+      const int units = M * segs;
+      for (int u = threadIdx.x; u < units; u += kWarpsC * 32) {
+        const int m = u / segs;
+        const int sg = u - m * segs;
+        const uint4* src = reinterpret_cast<const uint4*>(sAs + m * TK + sg * 16);
+        const uint4 v0 = src[0], v1 = src[1];
+        float4* row = reinterpret_cast<float4*>(fAt + m * TK);
+        row[fa_chunk(sg, 0)] = make_float4(bf16lo(v0.x) * F::prescale(0), bf16hi(v0.x) * F::prescale(1),
+                                           bf16lo(v0.y) * F::prescale(2), bf16hi(v0.y) * F::prescale(3));
+        row[fa_chunk(sg, 1)] = make_float4(bf16lo(v0.z) * F::prescale(4), bf16hi(v0.z) * F::prescale(5),
+                                           bf16lo(v0.w) * F::prescale(6), bf16hi(v0.w) * F::prescale(7));
+        row[fa_chunk(sg, 2)] = make_float4(bf16lo(v1.x) * F::prescale(8), bf16hi(v1.x) * F::prescale(9),
+                                           bf16lo(v1.y) * F::prescale(10), bf16hi(v1.y) * F::prescale(11));
+        row[fa_chunk(sg, 3)] = make_float4(bf16lo(v1.z) * F::prescale(12), bf16hi(v1.z) * F::prescale(13),
+                                           bf16lo(v1.w) * F::prescale(14), bf16hi(v1.w) * F::prescale(15));
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarpsC * 32) : "memory");
+    if (ok) {
       for (int sg = lane; sg < segs; sg += 32) {
-        Seg g;
-        F::decode(p, n, t, sg, sW, g);
-        seg_fma<M, F::kJ8>(g, sAs + sg * 16, kTileK, acc);
+        Seg g[kRowsPerWarp];
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+          if (r0 + r < rows) {
+            F::decode(p, n0 + r0 + r, t, sg, sW + (r0 + r) * F::kWRow, g[r]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) g[r].w[i] = make_float2(0.f, 0.f);
+            g[r].s = 0.f;
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const float4* row = reinterpret_cast<const float4*>(fAt + m * TK);
+          const float4 q0 = row[fa_chunk(sg, 0)], q1 = row[fa_chunk(sg, 1)];
+          const float4 q2 = row[fa_chunk(sg, 2)], q3 = row[fa_chunk(sg, 3)];
+          const float2 a[8] = {make_float2(q0.x, q0.y), make_float2(q0.z, q0.w),
+                               make_float2(q1.x, q1.y), make_float2(q1.z, q1.w),
+                               make_float2(q2.x, q2.y), make_float2(q2.z, q2.w),
+                               make_float2(q3.x, q3.y), make_float2(q3.z, q3.w)};
+#pragma unroll
+          for (int r = 0; r < kRowsPerWarp; ++r) {
+            float2 c0 = __fmul2_rn(a[0], g[r].w[0]);
+            float2 c1 = __fmul2_rn(a[4], g[r].w[4]);
+            c0 = __ffma2_rn(a[1], g[r].w[1], c0);
+            c1 = __ffma2_rn(a[5], g[r].w[5], c1);
+            c0 = __ffma2_rn(a[2], g[r].w[2], c0);
+            c1 = __ffma2_rn(a[6], g[r].w[6], c1);
+            c0 = __ffma2_rn(a[3], g[r].w[3], c0);
+            c1 = __ffma2_rn(a[7], g[r].w[7], c1);
+            acc[r][m] = __ffma2_rn(__fadd2_rn(c0, c1), f2(g[r].s), acc[r][m]);
+          }
+        }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
   }
-  if (!ok || !live) return;
+  if (!ok) return;
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const float v = warp_sum(acc[m]);
-    if (lane == m) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(v);
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int n = n0 + r0 + r;
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const float v = warp_sum(acc[r][m].x + acc[r][m].y);
+      if (lane == m && r0 + r < rows) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(v);
+    }
   }
-}
-
-template <class F, int M, bool BULK>
-constexpr int scalar_smem_bytes() {
-  constexpr int kStages = (M <= 4) ? 6 : (M <= 8 ? 4 : 3);
-  constexpr int kWStage = kRows * F::kWBytesPerRow;
-  constexpr int kAStage = M * kTileK * 2;
-  return kStages * (((kWStage + kAStage) + 127) / 128 * 128);
 }
 
 template <class F, int M, bool BULK>
 cudaError_t launch_scalar_m(const GemvArgs& a, cudaStream_t s) {
   auto kern = gemv_scalar_kernel<F, M, BULK>;
-  constexpr int smem = scalar_smem_bytes<F, M, BULK>();
+  constexpr int smem = ScalarCfg<F, M>::kSmem;
   static bool attr_set = false;  // idempotent; racing writers set the same value
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
