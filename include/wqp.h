@@ -75,6 +75,20 @@ int q2_gemv(const void* A, const void* W, const void* scales, void* C,
 int q2_gemv_strided(const void* A, int lda, const void* W, void* C, int ldc,
                     int M, int N, int K, void* stream);
 
+/* Tensor-core (tcgen05) form of q2_gemv: swap-AB, with the weight rows on
+ * the 128-row MMA side and the activation rows padded to 16 on the MMA N
+ * side. Every code - 1 is exact in BF16, so the products are exact. Each
+ * 128-K group's partial sum is scaled by its inline d once, in FP32.
+ * Arguments and layouts are those of q2_gemv, with two more limits:
+ * 1 <= M <= 16, and K % 1024 == 0, so that rows stay 16-byte aligned for the
+ * tensor-map copies. Anything else gives WQP_ERR_INVALID_ARG.
+ * Numerics: the contract is that of w8a16_gemm_tc. It is not bit-identical
+ * to q2_gemv. A row does not depend on the other rows of the call.
+ */
+int q2_gemm_tc(const void* A, const void* W, void* C, int M, int N, int K, void* stream);
+int q2_gemm_tc_strided(const void* A, int lda, const void* W, void* C, int ldc,
+                       int M, int N, int K, void* stream);
+
 /* ---------------------------------------------------------------- W4A16 ---
  * 4-bit E2M1 weights with E4M3 group scales (NVFP4-style) decode GEMV.
  * The family is "spark_model/layers/w4a16_gemv_tiers.rs" (module docs: the

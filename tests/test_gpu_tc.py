@@ -34,7 +34,10 @@ def _check_tc(oracle_lib, d, C, what):
     ref = G.run_oracle(oracle_lib, d)
     a = synth.bf16_bits_to_f32(d["A"]).astype(np.float64)
     a_rms = np.sqrt((a ** 2).mean(axis=1))
-    w_max = np.abs(oracle_lib.w8_dequant(d["W"], d["S"], d["N"], d["K"])).max(axis=1)
+    if d["fmt"] == "q2":
+        w_max = np.abs(oracle_lib.q2_dequant(d["W"], d["N"], d["K"])).max(axis=1)
+    else:
+        w_max = np.abs(oracle_lib.w8_dequant(d["W"], d["S"], d["N"], d["K"])).max(axis=1)
     ok = tc_ok(C, ref, d["K"], a_rms, w_max)
     bad = np.argwhere(~ok)
     assert bad.size == 0, (what, len(bad), bad[:3], bf16_to_f64(C[tuple(bad[0])]),
@@ -81,3 +84,49 @@ def test_tc_full_size(oracle_lib, N, K, Ms):
         C = G.host_bits(G.run_gpu(d, tc=True))
         frac = _check_tc(oracle_lib, d, C, f"full M={M} N={N} K={K}")
         assert frac > 0.99   # almost every output is also within the scalar 1-ULP term
+
+
+# ------------------------------------------------------------------ Q2_0
+@pytest.mark.parametrize("N,K", [(128, 1024), (200, 2048), (1000, 1024), (77, 3072), (384, 8192)])
+def test_q2_tc_parity_small(oracle_lib, N, K):
+    for M in (1, 4, 16):
+        d = G.make("q2", M, N, K, seed=500 + N + K + M)
+        C = G.host_bits(G.run_gpu(d, tc=True))
+        _check_tc(oracle_lib, d, C, f"q2 M={M} N={N} K={K}")
+
+
+def test_q2_tc_exact_arithmetic_bit_exact(oracle_lib):
+    """Codes -1/0/1 times small integers, power-of-two d: exact in any order."""
+    r = np.random.default_rng(8)
+    M, N, K = 16, 260, 3072
+    a = r.integers(-4, 5, size=(M, K)).astype(np.float32)
+    A = synth.bf16_bits_from_f32(a)
+    codes = r.integers(0, 3, size=(N, K), dtype=np.uint8)
+    dd = (2.0 ** -r.integers(2, 6, size=(N, K // 128))).astype(np.float16)
+    W = synth.pack_q2(codes, dd)
+    d = {"A": A, "dA": G.dev_bf16(A), "M": M, "N": N, "K": K, "fmt": "q2", "W": W, "dW": G.dev_u8(W)}
+    C = G.host_bits(G.run_gpu(d, tc=True))
+    assert np.array_equal(C, G.run_oracle(oracle_lib, d).c)
+
+
+def test_q2_tc_rows_independent_and_k_rule():
+    import weight_only_quantized_packed_gb300 as wqp
+
+    d = G.make("q2", 16, 5120, 5120, seed=21)
+    c16 = G.host_bits(G.run_gpu(d, tc=True))
+    for m in (0, 7, 15):
+        one = G.host_bits(G.run_gpu(d, tc=True, A=d["dA"][m:m + 1]))
+        assert np.array_equal(one[0], c16[m])
+    bad = G.make("q2", 1, 64, 640, seed=2)
+    with pytest.raises(wqp.WqpError):
+        G.run_gpu(bad, tc=True)          # K % 1024 != 0
+
+
+@pytest.mark.parametrize("N,K,Ms", [(5120, 5120, (1, 4, 8, 16)), (7168, 5120, (8,)),
+                                    (5120, 17408, (16,)), (34816, 5120, (4,))])
+def test_q2_tc_full_size(oracle_lib, N, K, Ms):
+    for M in Ms:
+        d = G.make("q2", M, N, K, seed=synth.seed_for(1, M))
+        C = G.host_bits(G.run_gpu(d, tc=True))
+        frac = _check_tc(oracle_lib, d, C, f"q2 full M={M} N={N} K={K}")
+        assert frac > 0.99

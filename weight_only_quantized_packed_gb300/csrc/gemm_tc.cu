@@ -1,23 +1,28 @@
-// Tensor-core (tcgen05) swap-AB decode GEMM for FP8 E4M3 weights with FP32
-// 128x128 block scales, 1 <= M <= 16
+// Tensor-core (tcgen05) swap-AB decode GEMM for packed weights, 1 <= M <= 16.
+//
+// FP8 E4M3 with FP32 128x128 block scales
 // ("metrale_model_layers/layers/ops/w8a16_gemm_m16.rs": doc of
 // `w8a16_gemm_m16` for the operands and the 16-row M tile; module docs for
 // the block scale being folded once per 128-K block onto an FP32 outer
-// accumulator, never per element and never into BF16).
+// accumulator, never per element and never into BF16), and ternary Q2_0 with
+// its inline fp16 scale per 128-K group ("spark_model/layers/ops/gemv_q2_vec.rs",
+// module docs), whose scale is folded the same way.
 //
-// Swap-AB: the 128 weight rows of a tile are the MMA's M side and the M <= 16
+// Swap-AB: the 128 weight rows of a tile are the MMA's M side, and the M <= 16
 // activation rows, zero-padded to 16, are its N side:
-//   D[n, m] = sum_k W[n, k] * A[m, k]     (tcgen05.mma kind::f16, M=128 N=16 K=16)
-// E4M3 values are exactly representable in BF16, so the products are exact.
-// The tensor core reduces each 16-K step in its own order, so the result is
-// not bit-identical to the scalar kernel.
+//   D[n, m] = sum_k W[n, k] * A[m, k]   (tcgen05.mma kind::f16, M=128 N=16 K=16)
+// Every E4M3 value and every Q2_0 code - 1 is exactly representable in BF16,
+// so the products are exact. The tensor core reduces each 16-K step in its
+// own order, so the result is not bit-identical to the scalar kernels. Each
+// output row still depends only on its own activation row.
 //
 // One CTA = one 128-row tile x a contiguous range of 128-K groups. Roles:
-//   warp 8      TMA: raw FP8 tiles [128 rows x 128 B] (128-byte swizzle) and
-//               activation tiles [16 rows x 64 K] x 2 (128-byte swizzle, rows
-//               past M are zero-filled), through mbarrier rings;
-//   warps 0..7  convert FP8 -> BF16 into the K-major, no-swizzle operand tile
-//               (8x16-byte core matrices), one row and half a group per thread;
+//   warp 8      TMA: raw weight tiles (FP8: [128 rows x 128 B] with 128-byte
+//               swizzle; Q2_0: [128 rows x 272 B] = 8 groups) and activation
+//               tiles [16 rows x 64 K] x 2 (128-byte swizzle, rows past M
+//               zero-filled), through mbarrier rings;
+//   warps 0..7  decode one row and half a group per thread into the K-major,
+//               no-swizzle BF16 operand tile (8 x 16-byte core matrices);
 //   warp 9      allocates TMEM and issues the 8 MMAs of each group into its
 //               own 16-column accumulator slot, then commits;
 //   warps 0..3  also fold each group: tcgen05.ld of the slot (lane = weight
@@ -37,39 +42,111 @@ namespace tc {
 
 constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int BN = 16;             // activation rows (MMA N)
-constexpr int GK = 128;            // K per group = block-scale granularity
+constexpr int GK = 128;            // K per group = scale granularity
 constexpr int kConvWarps = 8;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
-constexpr int SR = 6;              // raw stages (96 KB of weights in flight)
-constexpr int SA = 4;              // activation stages
+constexpr int SA = 8;              // activation stages (prefetched independently)
 constexpr int SO = 2;              // operand stages
 constexpr int NACC = 4;            // TMEM accumulator slots
 constexpr int LAG = NACC - 1;      // fold group j - LAG after converting group j
 constexpr uint32_t kTmemCols = 64; // NACC * 16, rounded to a power of two >= 32
-
 constexpr int kOpBytes = BM * GK * 2;      // 32 KB
-constexpr int kRawBytes = BM * GK;         // 16 KB (FP8)
 constexpr int kActBytes = BN * GK * 2;     // 4 KB
-constexpr int kOpOff = 0;
-constexpr int kRawOff = kOpOff + SO * kOpBytes;
-constexpr int kActOff = kRawOff + SR * kRawBytes;
-constexpr int kSmemBytes = kActOff + SA * kActBytes;
-constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack for 1024-byte alignment
-static_assert(BM * BN * 4 <= SR * kRawBytes, "split-K partials alias the raw ring");
 
 struct TcParams {
-  const float* scales;     // [ceil(N/128), K/128]
+  const float* scales;     // FP8: [ceil(N/128), K/128]; Q2_0: unused
   uint16_t* C;
   int M, N, K, ldc;
   int splits;              // CTAs per tile (cluster size)
+  int stages;              // raw stages per tile (K / (128 * GPR))
   unsigned* err;
 };
 
+// ------------------------------------------------------------------ formats
+// FP8 E4M3: one group per raw stage, [128 rows x 128 B], 128-byte swizzle.
+struct Fp8Tc {
+  static constexpr int kGPR = 1;
+  static constexpr int kSR = 6;
+  static constexpr int kRawBytes = BM * GK;
+  static constexpr bool kRowScale = false;
+  __device__ static void issue_raw(const CUtensorMap* m, uint32_t dst, int g0, int n0, uint32_t bar,
+                                   uint64_t pol) {
+    tma_load_2d_hint(dst, m, g0 * GK, n0, bar, pol);
+  }
+  // Row r, half h (64 K) of group gi of the raw stage -> operand row base op
+  // (core matrix (k8, r8) at k8 * 2048 + r8 * 128, row r % 8 at +16 r).
+  __device__ static void convert(const uint8_t* raw, int, int r, int h, uint8_t* op, float&) {
+    const uint8_t* row = raw + r * 128;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const int c = h * 4 + c4;                                    // 16-byte chunk = 16 K
+      const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+      uint4 lo, hi;
+      e4m3x4_to_bf16(v.x, lo.x, lo.y);
+      e4m3x4_to_bf16(v.y, lo.z, lo.w);
+      e4m3x4_to_bf16(v.z, hi.x, hi.y);
+      e4m3x4_to_bf16(v.w, hi.z, hi.w);
+      *reinterpret_cast<uint4*>(op + (2 * c) * 2048) = lo;
+      *reinterpret_cast<uint4*>(op + (2 * c + 1) * 2048) = hi;
+    }
+  }
+};
+
+// Q2_0: eight groups per raw stage, [128 rows x 8 blocks x 34 B], no swizzle.
+struct Q2Tc {
+  static constexpr int kGPR = 8;
+  static constexpr int kSR = 3;
+  static constexpr int kRawBytes = BM * 8 * 34;
+  static constexpr bool kRowScale = true;
+  __device__ static void issue_raw(const CUtensorMap* m, uint32_t dst, int g0, int n0, uint32_t bar,
+                                   uint64_t pol) {
+    tma_load_2d_hint(dst, m, g0 * 17, n0, bar, pol);              // 17 u16 per block
+  }
+  __device__ static void convert(const uint8_t* raw, int gi, int r, int h, uint8_t* op, float& d) {
+    const uint16_t* blk = reinterpret_cast<const uint16_t*>(raw + r * 272 + gi * 34);
+    if (h == 0) d = __half2float(__ushort_as_half(blk[16]));
+#pragma unroll
+    for (int w4 = 0; w4 < 4; ++w4) {
+      const int w = h * 4 + w4;                                    // 16-code word of the block
+      const uint32_t q = static_cast<uint32_t>(blk[2 * w]) | (static_cast<uint32_t>(blk[2 * w + 1]) << 16);
+      uint32_t p[8];
+      q2_decode_word(q, p);                                        // p[j] = (c_j - 1, c_{j+8} - 1)
+      uint4 lo, hi;                                                // natural pairs (c_2i, c_2i+1)
+      lo.x = __byte_perm(p[0], p[1], 0x5410);
+      lo.y = __byte_perm(p[2], p[3], 0x5410);
+      lo.z = __byte_perm(p[4], p[5], 0x5410);
+      lo.w = __byte_perm(p[6], p[7], 0x5410);
+      hi.x = __byte_perm(p[0], p[1], 0x7632);
+      hi.y = __byte_perm(p[2], p[3], 0x7632);
+      hi.z = __byte_perm(p[4], p[5], 0x7632);
+      hi.w = __byte_perm(p[6], p[7], 0x7632);
+      *reinterpret_cast<uint4*>(op + (2 * w) * 2048) = lo;         // k = 16 w .. 16 w + 7
+      *reinterpret_cast<uint4*>(op + (2 * w + 1) * 2048) = hi;     // k = 16 w + 8 .. + 15
+    }
+  }
+};
+
+template <class F>
+struct Layout {
+  static constexpr int kOpOff = 0;
+  static constexpr int kRawOff = kOpOff + SO * kOpBytes;
+  static constexpr int kActOff = (kRawOff + F::kSR * F::kRawBytes + 1023) / 1024 * 1024;
+  static constexpr int kSclOff = kActOff + SA * kActBytes;
+  static constexpr int kBytes = kSclOff + NACC * BM * 4;
+  static constexpr int kAlloc = kBytes + 1024;                     // slack for 1024-byte alignment
+  static_assert(BM * BN * 4 <= F::kSR * F::kRawBytes, "split-K partials alias the raw ring");
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+template <class F>
 __global__ void __launch_bounds__(kThreads, 1)
-    w8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
-                 TcParams p) {
+    tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+              TcParams p) {
+  using L = Layout<F>;
+  constexpr int SR = F::kSR;
+  constexpr int GPR = F::kGPR;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[SR], raw_empty[SR];
   __shared__ __align__(8) uint64_t act_full[SA], act_empty[SA];
@@ -86,10 +163,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tile = blockIdx.x / splits;
   const int rank = blockIdx.x - tile * splits;      // == %cluster_ctarank
   const int n0 = tile * BM;
-  const int G = p.K / GK;
-  const int g_begin = (rank * G) / splits;
-  const int g_end = ((rank + 1) * G) / splits;
-  const int ng = g_end - g_begin;
+  const int st_begin = (rank * p.stages) / splits;
+  const int st_end = ((rank + 1) * p.stages) / splits;
+  const int g_begin = st_begin * GPR;
+  const int ng = (st_end - st_begin) * GPR;          // groups of this CTA
+  const int nst = st_end - st_begin;                 // raw stages of this CTA
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
@@ -120,38 +198,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA
+    // Lane 0 streams raw weight stages, lane 1 streams activation tiles, so
+    // neither ring waits on the other.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int raw_issued = 0, act_issued = 0;
-      bool ok = true;
-      for (int j = 0; j < ng && j < SR; ++j) {
-        mbar_arrive_expect_tx(smem_u32(&raw_full[j]), kRawBytes);
-        tma_load_2d_hint(sbase + kRawOff + j * kRawBytes, &tmW, (g_begin + j) * GK, n0,
-                         smem_u32(&raw_full[j]), pol);
-        raw_issued = j + 1;
+      int raw_issued = 0;
+      for (int t = 0; t < nst; ++t) {
+        const int sr = t % SR;
+        if (t >= SR && !wait_or_abort(smem_u32(&raw_empty[sr]), ((t / SR) - 1) & 1, p.err, abort_flag)) break;
+        mbar_arrive_expect_tx(smem_u32(&raw_full[sr]), F::kRawBytes);
+        F::issue_raw(&tmW, sbase + L::kRawOff + sr * F::kRawBytes, g_begin + t * GPR, n0,
+                     smem_u32(&raw_full[sr]), pol);
+        raw_issued = t + 1;
       }
+      // Drain: every issued copy has landed before the CTA may exit.
+      for (int t = max(0, raw_issued - SR); t < raw_issued; ++t)
+        mbar_wait(smem_u32(&raw_full[t % SR]), (t / SR) & 1, p.err);
+    } else if (lane == 1) {
       pdl_wait();                          // activations may come from the previous kernel
-      for (int j = 0; j < ng && ok; ++j) {
+      int act_issued = 0;
+      for (int j = 0; j < ng; ++j) {
         const int sa = j % SA;
-        if (j >= SA && !(ok = wait_or_abort(smem_u32(&act_empty[sa]), ((j / SA) - 1) & 1, p.err, abort_flag))) break;
+        if (j >= SA && !wait_or_abort(smem_u32(&act_empty[sa]), ((j / SA) - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(smem_u32(&act_full[sa]), kActBytes);
-        const uint32_t dst = sbase + kActOff + sa * kActBytes;
+        const uint32_t dst = sbase + L::kActOff + sa * kActBytes;
         tma_load_2d(dst, &tmA, (g_begin + j) * GK, 0, smem_u32(&act_full[sa]));
         tma_load_2d(dst + kActBytes / 2, &tmA, (g_begin + j) * GK + 64, 0, smem_u32(&act_full[sa]));
         act_issued = j + 1;
-        const int jn = j + SR;
-        if (jn < ng) {
-          const int sr = jn % SR;
-          if (!(ok = wait_or_abort(smem_u32(&raw_empty[sr]), ((jn / SR) - 1) & 1, p.err, abort_flag))) break;
-          mbar_arrive_expect_tx(smem_u32(&raw_full[sr]), kRawBytes);
-          tma_load_2d_hint(sbase + kRawOff + sr * kRawBytes, &tmW, (g_begin + jn) * GK, n0,
-                           smem_u32(&raw_full[sr]), pol);
-          raw_issued = jn + 1;
-        }
       }
-      // Drain: every issued copy has landed before the CTA may exit.
-      for (int j = max(0, raw_issued - SR); j < raw_issued; ++j)
-        mbar_wait(smem_u32(&raw_full[j % SR]), (j / SR) & 1, p.err);
       for (int j = max(0, act_issued - SA); j < act_issued; ++j)
         mbar_wait(smem_u32(&act_full[j % SA]), (j / SA) & 1, p.err);
     }
@@ -166,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_or_abort(smem_u32(&act_full[sa]), (j / SA) & 1, p.err, abort_flag)) break;
         if (j >= NACC && !wait_or_abort(smem_u32(&acc_empty[sc]), ((j / NACC) - 1) & 1, p.err, abort_flag)) break;
         tc_fence_after();
-        const uint32_t opb = sbase + kOpOff + so * kOpBytes;
-        const uint32_t actb = sbase + kActOff + sa * kActBytes;
+        const uint32_t opb = sbase + L::kOpOff + so * kOpBytes;
+        const uint32_t actb = sbase + L::kActOff + sa * kActBytes;
 #pragma unroll
         for (int i = 0; i < GK / 16; ++i) {
           // Operand: core matrix (k8, r8) at (k8 * 16 + r8) * 128 B; one MMA
@@ -195,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp >> 2;                // which 64-K half of a group
     const int r = q * 32 + lane;            // row within the tile
     const bool folds = warp < 4;
-    const float* srow = p.scales + static_cast<size_t>(tile) * G;   // 128-row tiles == scale rows
+    float* scl = reinterpret_cast<float*>(smem + L::kSclOff);     // [NACC][BM] row scales
+    const float* srow = F::kRowScale ? nullptr : p.scales + static_cast<size_t>(tile) * (p.K / GK);
     int folded = 0;
     auto fold = [&](int j) -> bool {
       const int sc = j % NACC;
@@ -208,36 +283,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[sc]));
-      const float s = __ldg(srow + g_begin + j);
+      const float s = F::kRowScale ? scl[sc * BM + r] : __ldg(srow + g_begin + j);
 #pragma unroll
       for (int m = 0; m < BN; ++m) acc[m] = fmaf(v[m], s, acc[m]);
       return true;
     };
     bool ok = true;
     for (int j = 0; j < ng && ok; ++j) {
-      const int sr = j % SR, so = j % SO;
-      const bool g1 = wait_or_abort(smem_u32(&raw_full[sr]), (j / SR) & 1, p.err, abort_flag);
+      const int t = j / GPR, gi = j % GPR;
+      const int sr = t % SR, so = j % SO;
+      const bool g1 = (gi != 0) || wait_or_abort(smem_u32(&raw_full[sr]), (t / SR) & 1, p.err, abort_flag);
       const bool g2 = g1 && (j < SO || wait_or_abort(smem_u32(&op_empty[so]), ((j / SO) - 1) & 1, p.err, abort_flag));
       if (!__all_sync(0xFFFFFFFFu, g1 && g2)) { ok = false; break; }
-      const uint8_t* raw = smem + kRawOff + sr * kRawBytes + r * 128;
-      uint8_t* op = smem + kOpOff + so * kOpBytes + (r >> 3) * 128 + (r & 7) * 16;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int c = h * 4 + c4;                                   // 16-byte chunk = 16 K
-        const uint4 v = *reinterpret_cast<const uint4*>(raw + ((c ^ (r & 7)) << 4));
-        uint4 lo, hi;
-        e4m3x4_to_bf16(v.x, lo.x, lo.y);
-        e4m3x4_to_bf16(v.y, lo.z, lo.w);
-        e4m3x4_to_bf16(v.z, hi.x, hi.y);
-        e4m3x4_to_bf16(v.w, hi.z, hi.w);
-        *reinterpret_cast<uint4*>(op + (2 * c) * 2048) = lo;        // core matrix k8 = 2c
-        *reinterpret_cast<uint4*>(op + (2 * c + 1) * 2048) = hi;    // k8 = 2c + 1
-      }
+      float d = 0.0f;
+      F::convert(smem + L::kRawOff + sr * F::kRawBytes, gi, r, h,
+                 smem + L::kOpOff + so * kOpBytes + (r >> 3) * 128 + (r & 7) * 16, d);
+      if (F::kRowScale && h == 0) scl[(j % NACC) * BM + r] = d;   // read back by this thread's fold
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&op_full[so]));
-        mbar_arrive(smem_u32(&raw_empty[sr]));
+        if (gi == GPR - 1) mbar_arrive(smem_u32(&raw_empty[sr]));
       }
       if (folds && j >= LAG) {
         if (!fold(j - LAG)) { ok = false; break; }
@@ -252,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------- reduce + store
   __syncthreads();
   const bool failed = *abort_flag != 0;
-  float* red = reinterpret_cast<float*>(smem + kRawOff);   // raw ring is idle now
+  float* red = reinterpret_cast<float*>(smem + L::kRawOff);   // raw ring is idle now
   if (splits > 1) {
     if (warp < 4 && rank != 0) {
       float4* dst = reinterpret_cast<float4*>(red + (warp * 32 + lane) * BN);
@@ -262,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();
     if (warp < 4 && rank == 0) {
       const uint32_t mine = smem_u32(red + (warp * 32 + lane) * BN);
-      for (int q = 1; q < splits; ++q) {
-        const uint32_t rem = mapa_shared(mine, q);
+      for (int qq = 1; qq < splits; ++qq) {
+        const uint32_t rem = mapa_shared(mine, qq);
 #pragma unroll
         for (int i = 0; i < BN / 4; ++i) {
           const float4 v = ld_dsmem_f4(rem + 16 * i);
@@ -278,8 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp < 4 && rank == 0 && !failed) {
     const int n = n0 + warp * 32 + lane;
-    if (n < p.N)
-      for (int m = 0; m < p.M; ++m) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc[m]);
+    if (n < p.N) {
+#pragma unroll
+      for (int m = 0; m < BN; ++m)
+        if (m < p.M) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc[m]);
+    }
   }
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -317,35 +386,29 @@ cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int choose_splits(int tiles, int groups, int num_sms) {
+int choose_splits(int tiles, int stages, int num_sms) {
   int s = num_sms / tiles;                   // one CTA per SM, a single wave
   if (s < 1) s = 1;
   if (s > 8) s = 8;                          // portable cluster size
-  if (s > groups) s = groups;
+  if (s > stages) s = stages;
   return s;
 }
 
-}  // namespace tc
-
-cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s) {
-  using namespace tc;
-  CUtensorMap mw, ma;
-  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, static_cast<uint64_t>(a.K),
-                              static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K), GK, BM,
+template <class F>
+cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, cudaStream_t s) {
+  using L = Layout<F>;
+  CUtensorMap ma;
+  cudaError_t e = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, static_cast<uint64_t>(a.K),
+                              static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda) * 2, 64, BN,
                               CU_TENSOR_MAP_SWIZZLE_128B);
-  if (e != cudaSuccess) return e;
-  e = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, static_cast<uint64_t>(a.K),
-                  static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda) * 2, 64, BN,
-                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   static bool attr_set = false;
   if (!attr_set) {
-    e = cudaFuncSetAttribute(w8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    e = cudaFuncSetAttribute(tc_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int tiles = (a.N + BM - 1) / BM;
-  const int G = a.K / GK;
   TcParams p;
   p.scales = static_cast<const float*>(a.scales);
   p.C = static_cast<uint16_t*>(a.C);
@@ -353,13 +416,14 @@ cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s) {
   p.N = a.N;
   p.K = a.K;
   p.ldc = a.ldc;
-  p.splits = choose_splits(tiles, G, a.num_sms);
+  p.stages = a.K / (GK * F::kGPR);
+  p.splits = choose_splits(tiles, p.stages, a.num_sms);
   p.err = a.err;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * p.splits);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -375,7 +439,32 @@ cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, w8_tc_kernel, mw, ma, p);
+  return cudaLaunchKernelEx(&cfg, tc_kernel<F>, mw, ma, p);
+}
+
+}  // namespace tc
+
+cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mw;
+  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, static_cast<uint64_t>(a.K),
+                              static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K), GK, BM,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  return launch_tc<Fp8Tc>(a, mw, s);
+}
+
+// Requires K % 1024 == 0 (checked by the caller): a row is then 34 * K / 128
+// bytes, a multiple of 16, and each raw stage of 8 groups starts on a
+// 16-byte boundary.
+cudaError_t launch_q2_gemm_tc(const GemvArgs& a, cudaStream_t s) {
+  using namespace tc;
+  const uint64_t G = static_cast<uint64_t>(a.K / GK);
+  CUtensorMap mw;
+  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),
+                              34 * G, 8 * 17, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  return launch_tc<Q2Tc>(a, mw, s);
 }
 
 }  // namespace wqp
