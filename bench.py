@@ -135,6 +135,22 @@ def committed_traffic(kernel_key):
     return None
 
 
+def reduce_max_ms(ms: float, dist=None, device="cuda") -> float:
+    """Slowest rank's time (max over ranks); identity without a group."""
+    if dist is None:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_per_step: int, steps: int, world: int, ms_total_max: float) -> float:
+    """Whole-job GB/s: all ranks' weight bytes over the slowest rank's time."""
+    return world * bytes_per_step * steps / (ms_total_max * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ GPU arm
 class Workload:
     """Device-resident inputs for one format/shape, weights cycled over
@@ -315,12 +331,9 @@ def gpu_arm(args, rank, world, local_rank):
             for (a, b), M in zip(ev[s], H["Ms"]):
                 per[M].append(a.elapsed_time(b) * 1e3)
     wqp.set_pdl(False)
-    t = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total = float(t.item())
+    ms_total = reduce_max_ms(ms_total, dist)
     ms_step = ms_total / args.steps
-    value = world * bytes_step * args.steps / (ms_total * 1e-3) / 1e9
+    value = job_value(bytes_step, args.steps, world, ms_total)
 
     # Dominant kernel: the call with the largest average duration.
     avg = {M: statistics.fmean(v) for M, v in per.items()}

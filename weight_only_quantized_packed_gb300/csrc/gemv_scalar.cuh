@@ -9,11 +9,11 @@
 //               word is read once for all M rows (doc of
 //               `q2_0_gemv_vec_batchm`) and every activation load serves two
 //               weight rows;
-//   warp 8      producer: one lane streams the CTA's 16-row weight slab and
-//               the M BF16 activation rows through a STAGES-deep ring of K
-//               tiles with non-multicast bulk copies (cp.async.bulk) and
-//               mbarriers. If the rows are not 16-byte aligned, the whole
-//               producer warp copies with plain loads instead.
+//   warp 8      producer: streams the CTA's 16-row weight slab and the M
+//               BF16 activation rows through a STAGES-deep ring of K tiles
+//               with non-multicast bulk copies (cp.async.bulk, one lane per
+//               row, issued in parallel) and mbarriers. If the rows are not
+//               16-byte aligned, the producer warp copies with plain loads.
 // Per K tile the consumers first widen the activation tile to FP32 in shared
 // memory (double-buffered, one named barrier per tile), then stream the
 // weight segments.
@@ -34,6 +34,7 @@ constexpr int kWarpsC = 8;                  // consumer warps
 constexpr int kRowsPerWarp = 2;
 constexpr int kRows = kWarpsC * kRowsPerWarp;  // output rows per CTA
 constexpr int kThreads = (kWarpsC + 1) * 32;
+static_assert(kRows + 16 <= 32, "producer lanes: one per weight row, then one per activation row");
 
 __device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
 
@@ -131,15 +132,19 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
         __threadfence_block();
         __syncwarp();
       }
+      // One lane posts the stage's byte count, then the copies are issued in
+      // parallel: lane r < 16 copies weight row r, lane 16 + m activation row m.
       if (lane == 0) {
         const uint32_t tx = (BULK ? F::row_tile_bytes(tg) * rows : 0u) + abytes * M;
         mbar_arrive_expect_tx(fb, tx);
-        if (BULK)
-          for (int r = 0; r < rows; ++r)
-            F::issue_row_bulk(p, n0 + r, t, tg, smem_u32(sW + r * F::kWRow), fb, pol);
+      }
+      __syncwarp();
+      if (BULK && lane < rows)
+        F::issue_row_bulk(p, n0 + lane, t, tg, smem_u32(sW + lane * F::kWRow), fb, pol);
+      if (lane >= kRows && lane - kRows < M) {
+        const int m = lane - kRows;
         if (t == 0) pdl_wait();            // activations may come from the previous kernel
-        for (int m = 0; m < M; ++m)
-          bulk_g2s(smem_u32(sAs + m * TK * 2), p.A + static_cast<size_t>(m) * p.lda + t * TK, abytes, fb);
+        bulk_g2s(smem_u32(sAs + m * TK * 2), p.A + static_cast<size_t>(m) * p.lda + t * TK, abytes, fb);
       }
       issued = t + 1;
     }
