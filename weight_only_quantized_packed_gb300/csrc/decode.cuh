@@ -112,10 +112,19 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
 }
 
+// f16x2 -> bf16x2 for values whose FP32 form has a zero low half (every
+// E4M3 and E2M1 value): widen exactly to FP32, then keep the upper halves.
+// This avoids the FP32 -> BF16 packing conversion, which is slow.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_exact(uint32_t h) {
+  const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+}
+
 // Four E4M3 bytes of word x -> two bf16x2 pairs in element order.
 __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t x, uint32_t& p01, uint32_t& p23) {
-  p01 = f16x2_to_bf16x2(e4m3x2_to_f16x2(x & 0xFFFFu));
-  p23 = f16x2_to_bf16x2(e4m3x2_to_f16x2(x >> 16));
+  p01 = f16x2_to_bf16x2_exact(e4m3x2_to_f16x2(x & 0xFFFFu));
+  p23 = f16x2_to_bf16x2_exact(e4m3x2_to_f16x2(x >> 16));
 }
 
 // Four bytes = eight E2M1 codes of word x -> four bf16x2 pairs in element order.

@@ -17,23 +17,20 @@
 // output row still depends only on its own activation row.
 //
 // One CTA = one 128-row tile x a contiguous range of 128-K groups. Roles:
-//   warp 8      TMA: raw weight tiles (FP8: [128 rows x 128 B] with 128-byte
+//   warp 20     TMA: raw weight tiles (FP8: [128 rows x 128 B] with 128-byte
 //               swizzle; Q2_0: [128 rows x 272 B] = 8 groups) and activation
 //               tiles [16 rows x 64 K] x 2 (128-byte swizzle, rows past M
 //               zero-filled), through mbarrier rings;
-//   warps 0..7  decode one row and half a group per thread into the K-major,
-//               no-swizzle BF16 operand tile (8 x 16-byte core matrices);
-//   warp 9      allocates TMEM and issues the 8 MMAs of each group into its
+//   warps 0..15 decode one row and a quarter group (32 K) per thread into the
+//               K-major BF16 operand tile (128-byte swizzle, like the
+//               activations);
+//   warp 21     allocates TMEM and issues the 8 MMAs of each group into its
 //               own 16-column accumulator slot, then commits;
-//   warps 0..3  also fold each group: tcgen05.ld of the slot (lane = weight
-//               row, column = activation row), acc[m] += s * D[m] in FP32.
+//   warps 16..19 fold each group: tcgen05.ld of the slot (lane = weight row,
+//               column = activation row), acc[m] += s * D[m] in FP32.
 // When N is small, K is split over a thread-block cluster of up to 8 CTAs.
 // The partial sums are added in rank order through distributed shared memory
 // (deterministic, no global scratch).
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "decode.cuh"
 #include "tc.cuh"
 
@@ -43,14 +40,14 @@ namespace tc {
 constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int BN = 16;             // activation rows (MMA N)
 constexpr int GK = 128;            // K per group = scale granularity
-constexpr int kConvWarps = 8;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kConvWarps = 16;     // converters: row quarter = warp % 4, K quarter = warp / 4
+constexpr int kEpiWarp0 = 16;      // epilogue warps 16..19 (TMEM lane quarter = warp % 4)
+constexpr int kTmaWarp = 20;
+constexpr int kMmaWarp = 21;
+constexpr int kThreads = 22 * 32;
 constexpr int SA = 8;              // activation stages (prefetched independently)
-constexpr int SO = 2;              // operand stages
 constexpr int NACC = 4;            // TMEM accumulator slots
-constexpr int LAG = NACC - 1;      // fold group j - LAG after converting group j
+constexpr int NSCL = 8;            // row-scale ring (Q2_0 d), deeper than SO + NACC
 constexpr uint32_t kTmemCols = 64; // NACC * 16, rounded to a power of two >= 32
 constexpr int kOpBytes = BM * GK * 2;      // 32 KB
 constexpr int kActBytes = BN * GK * 2;     // 4 KB
@@ -64,32 +61,40 @@ struct TcParams {
   unsigned* err;
 };
 
+// Operand layout: a group's 128 rows x 128 K BF16 tile is two K-major blocks
+// of 64 K, each [128 rows x 128 B] with the 128-byte swizzle (16-byte chunk c
+// of row r stored at chunk c ^ (r % 8); 8-row atoms of 1024 B). cc is the
+// 8-K chunk index within the group (0..15).
+__device__ __forceinline__ uint8_t* op_chunk(uint8_t* op, int r, int cc) {
+  return op + (cc >> 3) * (BM * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+}
+
 // ------------------------------------------------------------------ formats
 // FP8 E4M3: one group per raw stage, [128 rows x 128 B], 128-byte swizzle.
 struct Fp8Tc {
   static constexpr int kGPR = 1;
-  static constexpr int kSR = 6;
+  static constexpr int kSR = 4;
+  static constexpr int kSO = 3;
   static constexpr int kRawBytes = BM * GK;
   static constexpr bool kRowScale = false;
   __device__ static void issue_raw(const CUtensorMap* m, uint32_t dst, int g0, int n0, uint32_t bar,
                                    uint64_t pol) {
     tma_load_2d_hint(dst, m, g0 * GK, n0, bar, pol);
   }
-  // Row r, half h (64 K) of group gi of the raw stage -> operand row base op
-  // (core matrix (k8, r8) at k8 * 2048 + r8 * 128, row r % 8 at +16 r).
-  __device__ static void convert(const uint8_t* raw, int, int r, int h, uint8_t* op, float&) {
+  // Row r, K quarter kq (32 K) of group gi of the raw stage -> operand stage op.
+  __device__ static void convert(const uint8_t* raw, int, int r, int kq, uint8_t* op, float&) {
     const uint8_t* row = raw + r * 128;
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      const int c = h * 4 + c4;                                    // 16-byte chunk = 16 K
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int c = kq * 2 + c2;                                   // 16-byte chunk = 16 K
       const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
       uint4 lo, hi;
       e4m3x4_to_bf16(v.x, lo.x, lo.y);
       e4m3x4_to_bf16(v.y, lo.z, lo.w);
       e4m3x4_to_bf16(v.z, hi.x, hi.y);
       e4m3x4_to_bf16(v.w, hi.z, hi.w);
-      *reinterpret_cast<uint4*>(op + (2 * c) * 2048) = lo;
-      *reinterpret_cast<uint4*>(op + (2 * c + 1) * 2048) = hi;
+      *reinterpret_cast<uint4*>(op_chunk(op, r, 2 * c)) = lo;
+      *reinterpret_cast<uint4*>(op_chunk(op, r, 2 * c + 1)) = hi;
     }
   }
 };
@@ -97,19 +102,20 @@ struct Fp8Tc {
 // Q2_0: eight groups per raw stage, [128 rows x 8 blocks x 34 B], no swizzle.
 struct Q2Tc {
   static constexpr int kGPR = 8;
-  static constexpr int kSR = 3;
+  static constexpr int kSR = 2;
+  static constexpr int kSO = 3;
   static constexpr int kRawBytes = BM * 8 * 34;
   static constexpr bool kRowScale = true;
   __device__ static void issue_raw(const CUtensorMap* m, uint32_t dst, int g0, int n0, uint32_t bar,
                                    uint64_t pol) {
     tma_load_2d_hint(dst, m, g0 * 17, n0, bar, pol);              // 17 u16 per block
   }
-  __device__ static void convert(const uint8_t* raw, int gi, int r, int h, uint8_t* op, float& d) {
+  __device__ static void convert(const uint8_t* raw, int gi, int r, int kq, uint8_t* op, float& d) {
     const uint16_t* blk = reinterpret_cast<const uint16_t*>(raw + r * 272 + gi * 34);
-    if (h == 0) d = __half2float(__ushort_as_half(blk[16]));
+    if (kq == 0) d = __half2float(__ushort_as_half(blk[16]));
 #pragma unroll
-    for (int w4 = 0; w4 < 4; ++w4) {
-      const int w = h * 4 + w4;                                    // 16-code word of the block
+    for (int w2 = 0; w2 < 2; ++w2) {
+      const int w = kq * 2 + w2;                                   // 16-code word of the block
       const uint32_t q = static_cast<uint32_t>(blk[2 * w]) | (static_cast<uint32_t>(blk[2 * w + 1]) << 16);
       uint32_t p[8];
       q2_decode_word(q, p);                                        // p[j] = (c_j - 1, c_{j+8} - 1)
@@ -122,8 +128,8 @@ struct Q2Tc {
       hi.y = __byte_perm(p[2], p[3], 0x7632);
       hi.z = __byte_perm(p[4], p[5], 0x7632);
       hi.w = __byte_perm(p[6], p[7], 0x7632);
-      *reinterpret_cast<uint4*>(op + (2 * w) * 2048) = lo;         // k = 16 w .. 16 w + 7
-      *reinterpret_cast<uint4*>(op + (2 * w + 1) * 2048) = hi;     // k = 16 w + 8 .. + 15
+      *reinterpret_cast<uint4*>(op_chunk(op, r, 2 * w)) = lo;      // k = 16 w .. 16 w + 7
+      *reinterpret_cast<uint4*>(op_chunk(op, r, 2 * w + 1)) = hi;  // k = 16 w + 8 .. + 15
     }
   }
 };
@@ -131,10 +137,11 @@ struct Q2Tc {
 template <class F>
 struct Layout {
   static constexpr int kOpOff = 0;
-  static constexpr int kRawOff = kOpOff + SO * kOpBytes;
+  static constexpr int kRawOff = kOpOff + F::kSO * kOpBytes;
   static constexpr int kActOff = (kRawOff + F::kSR * F::kRawBytes + 1023) / 1024 * 1024;
   static constexpr int kSclOff = kActOff + SA * kActBytes;
-  static constexpr int kBytes = kSclOff + NACC * BM * 4;
+  static constexpr int kBytes = kSclOff + NSCL * BM * 4;
+  static_assert(NSCL > F::kSO + NACC, "row-scale ring must outlive the pipeline");
   static constexpr int kAlloc = kBytes + 1024;                     // slack for 1024-byte alignment
   static_assert(BM * BN * 4 <= F::kSR * F::kRawBytes, "split-K partials alias the raw ring");
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -146,12 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               TcParams p) {
   using L = Layout<F>;
   constexpr int SR = F::kSR;
+  constexpr int SO = F::kSO;
   constexpr int GPR = F::kGPR;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[SR], raw_empty[SR];
   __shared__ __align__(8) uint64_t act_full[SA], act_empty[SA];
   __shared__ __align__(8) uint64_t op_full[SO], op_empty[SO];
   __shared__ __align__(8) uint64_t acc_full[NACC], acc_empty[NACC];
+  __shared__ __align__(8) uint64_t scl_full[NSCL];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -175,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < SA; ++i) { mbar_init(smem_u32(&act_full[i]), 1); mbar_init(smem_u32(&act_empty[i]), 1); }
     for (int i = 0; i < SO; ++i) { mbar_init(smem_u32(&op_full[i]), kConvWarps); mbar_init(smem_u32(&op_empty[i]), 1); }
     for (int i = 0; i < NACC; ++i) { mbar_init(smem_u32(&acc_full[i]), 1); mbar_init(smem_u32(&acc_empty[i]), 4); }
+    for (int i = 0; i < NSCL; ++i) mbar_init(smem_u32(&scl_full[i]), 4);
     abort_sh = 0;
     mbar_fence_init();
   }
@@ -244,9 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t actb = sbase + L::kActOff + sa * kActBytes;
 #pragma unroll
         for (int i = 0; i < GK / 16; ++i) {
-          // Operand: core matrix (k8, r8) at (k8 * 16 + r8) * 128 B; one MMA
-          // covers k8 = 2i, 2i+1: LBO (K step) = 2048 B, SBO (8-row step) = 128 B.
-          const uint64_t ad = sdesc(opb + i * 4096, 2048, 128, 0);
+          // Weights: 128-byte swizzled K-major blocks of 64 K (see op_chunk);
+          // 32 B per 16-K step; SBO = 1024 B (8-row atoms).
+          const uint64_t ad = sdesc(opb + (i >> 2) * (BM * 128) + (i & 3) * 32, 16, 1024, 2);
           // Activations: 128-byte swizzled rows of 64 K; 32 B per 16-K step,
           // the second 64 K in the second box; SBO = 1024 B (8-row atoms).
           const uint64_t bd = sdesc(actb + (i >> 2) * (kActBytes / 2) + (i & 3) * 32, 16, 1024, 2);
@@ -263,56 +273,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&acc_full[j % NACC]), (j / NACC) & 1, p.err);
       }
     }
-  } else {
-    // ------------------------------------------------------ convert (+ fold)
-    const int q = warp & 3;                 // TMEM lane quarter / row block
-    const int h = warp >> 2;                // which 64-K half of a group
+  } else if (warp < kConvWarps) {
+    // ------------------------------------------------------------ convert
+    const int q = warp & 3;                 // row block
+    const int kq = warp >> 2;               // which 32-K quarter of a group
     const int r = q * 32 + lane;            // row within the tile
-    const bool folds = warp < 4;
-    float* scl = reinterpret_cast<float*>(smem + L::kSclOff);     // [NACC][BM] row scales
+    float* scl = reinterpret_cast<float*>(smem + L::kSclOff);     // [NSCL][BM] row scales
+    for (int j = 0; j < ng; ++j) {
+      const int t = j / GPR, gi = j % GPR;
+      const int sr = t % SR, so = j % SO;
+      const bool g1 = (gi != 0) || wait_or_abort(smem_u32(&raw_full[sr]), (t / SR) & 1, p.err, abort_flag);
+      const bool g2 = g1 && (j < SO || wait_or_abort(smem_u32(&op_empty[so]), ((j / SO) - 1) & 1, p.err, abort_flag));
+      if (!__all_sync(0xFFFFFFFFu, g1 && g2)) break;
+      float d = 0.0f;
+      F::convert(smem + L::kRawOff + sr * F::kRawBytes, gi, r, kq, smem + L::kOpOff + so * kOpBytes, d);
+      // Slot j % NSCL is free: its previous group was folded before this
+      // group's operand stage could be released (pipeline depth SO + NACC).
+      if (F::kRowScale && kq == 0) scl[(j % NSCL) * BM + r] = d;
+      fence_proxy_async_smem();
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&op_full[so]));
+        if (gi == GPR - 1) mbar_arrive(smem_u32(&raw_empty[sr]));
+        if (F::kRowScale && kq == 0) mbar_arrive(smem_u32(&scl_full[j % NSCL]));
+      }
+    }
+  } else if (warp < kEpiWarp0 + 4) {
+    // ------------------------------------------------------------ fold
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int r = q * 32 + lane;
+    const float* scl = reinterpret_cast<const float*>(smem + L::kSclOff);
     const float* srow = F::kRowScale ? nullptr : p.scales + static_cast<size_t>(tile) * (p.K / GK);
-    int folded = 0;
-    auto fold = [&](int j) -> bool {
+    for (int j = 0; j < ng; ++j) {
       const int sc = j % NACC;
       // Warp-uniform outcome: tcgen05.ld below is .sync.aligned.
       const bool got = wait_or_abort(smem_u32(&acc_full[sc]), (j / NACC) & 1, p.err, abort_flag);
-      if (!__all_sync(0xFFFFFFFFu, got)) return false;
+      if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
       float v[16];
       tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + sc * 16, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[sc]));
-      const float s = F::kRowScale ? scl[sc * BM + r] : __ldg(srow + g_begin + j);
+      float s;
+      if (F::kRowScale) {
+        const bool gs = wait_or_abort(smem_u32(&scl_full[j % NSCL]), (j / NSCL) & 1, p.err, abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, gs)) break;
+        s = scl[(j % NSCL) * BM + r];
+      } else {
+        s = __ldg(srow + g_begin + j);
+      }
 #pragma unroll
       for (int m = 0; m < BN; ++m) acc[m] = fmaf(v[m], s, acc[m]);
-      return true;
-    };
-    bool ok = true;
-    for (int j = 0; j < ng && ok; ++j) {
-      const int t = j / GPR, gi = j % GPR;
-      const int sr = t % SR, so = j % SO;
-      const bool g1 = (gi != 0) || wait_or_abort(smem_u32(&raw_full[sr]), (t / SR) & 1, p.err, abort_flag);
-      const bool g2 = g1 && (j < SO || wait_or_abort(smem_u32(&op_empty[so]), ((j / SO) - 1) & 1, p.err, abort_flag));
-      if (!__all_sync(0xFFFFFFFFu, g1 && g2)) { ok = false; break; }
-      float d = 0.0f;
-      F::convert(smem + L::kRawOff + sr * F::kRawBytes, gi, r, h,
-                 smem + L::kOpOff + so * kOpBytes + (r >> 3) * 128 + (r & 7) * 16, d);
-      if (F::kRowScale && h == 0) scl[(j % NACC) * BM + r] = d;   // read back by this thread's fold
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&op_full[so]));
-        if (gi == GPR - 1) mbar_arrive(smem_u32(&raw_empty[sr]));
-      }
-      if (folds && j >= LAG) {
-        if (!fold(j - LAG)) { ok = false; break; }
-        folded = j - LAG + 1;
-      }
     }
-    if (folds && ok)
-      for (int j = folded; j < ng; ++j)
-        if (!fold(j)) { ok = false; break; }
   }
 
   // ---------------------------------------------------------- reduce + store
@@ -320,14 +334,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool failed = *abort_flag != 0;
   float* red = reinterpret_cast<float*>(smem + L::kRawOff);   // raw ring is idle now
   if (splits > 1) {
-    if (warp < 4 && rank != 0) {
-      float4* dst = reinterpret_cast<float4*>(red + (warp * 32 + lane) * BN);
+    const bool epi = warp >= kEpiWarp0 && warp < kEpiWarp0 + 4;
+    const int er = (warp - kEpiWarp0) * 32 + lane;
+    if (epi && rank != 0) {
+      float4* dst = reinterpret_cast<float4*>(red + er * BN);
 #pragma unroll
       for (int i = 0; i < BN / 4; ++i) dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
     }
     cluster_sync();
-    if (warp < 4 && rank == 0) {
-      const uint32_t mine = smem_u32(red + (warp * 32 + lane) * BN);
+    if (epi && rank == 0) {
+      const uint32_t mine = smem_u32(red + er * BN);
       for (int qq = 1; qq < splits; ++qq) {
         const uint32_t rem = mapa_shared(mine, qq);
 #pragma unroll
@@ -342,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cluster_sync();                       // remote partials stay alive until read
   }
-  if (warp < 4 && rank == 0 && !failed) {
-    const int n = n0 + warp * 32 + lane;
+  if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4 && rank == 0 && !failed) {
+    const int n = n0 + (warp - kEpiWarp0) * 32 + lane;
     if (n < p.N) {
 #pragma unroll
       for (int m = 0; m < BN; ++m)
@@ -358,34 +374,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                        CUtensorMapSwizzle sw) {
-  auto fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 int choose_splits(int tiles, int stages, int num_sms) {
   int s = num_sms / tiles;                   // one CTA per SM, a single wave
   if (s < 1) s = 1;

@@ -8,16 +8,19 @@ namespace wqp {
 struct Q2Fmt {
   static constexpr int kTK = 1024;                 // 8 groups per stage
   static constexpr int kWRow = 8 * 34;             // 8 blocks x 34 bytes
-  // Row tiles start at byte 34 * (n * K/128 + 8 t); 16-byte aligned for every
-  // n iff K/128 is a multiple of 8.
+  static constexpr int kW2Row = 0;
+  // A row is 34 * K/128 bytes: a multiple of 16 (as tensor maps need) iff
+  // K/128 is a multiple of 8.
   static bool bulk_ok(int K) { return (K / 128) % 8 == 0; }
-  __device__ static uint32_t row_tile_bytes(int tg) { return 34u * tg; }
-  __device__ static void issue_row_bulk(const ScalarParams& p, int n, int t, int tg, uint32_t dst,
-                                        uint32_t bar, uint64_t pol) {
-    const size_t G = static_cast<size_t>(p.K >> 7);
-    bulk_g2s_stream(dst, p.W + (n * G + 8 * t) * 34, 34u * tg, bar, pol);
+  static cudaError_t make_maps(const GemvArgs& a, CUtensorMap* mw, CUtensorMap*) {
+    const uint64_t row = 34ull * (a.K / 128);
+    return make_rows_map(mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, row / 4, a.N, row, kWRow / 4, kRows);
   }
-  __device__ static void copy_row_plain(const ScalarParams& p, int n, int t, int tg, uint8_t* dst,
+  __device__ static void issue_tile(const CUtensorMap* mw, const CUtensorMap*, uint32_t dst, uint32_t,
+                                    int t, int n0, uint32_t bar, uint64_t pol) {
+    tc::tma_load_2d_hint(dst, mw, t * (kWRow / 4), n0, bar, pol);
+  }
+  __device__ static void copy_row_plain(const ScalarParams& p, int n, int t, int tg, uint8_t* dst, uint8_t*,
                                         int lane) {
     const size_t G = static_cast<size_t>(p.K >> 7);
     const uint16_t* src = reinterpret_cast<const uint16_t*>(p.W + (n * G + 8 * t) * 34);
@@ -28,7 +31,8 @@ struct Q2Fmt {
   // inverse of the decoded weight's position factor (see q2_decode_f32).
   __device__ static constexpr float prescale(int pos) { return 1.0f / q2_pos_weight(pos); }
   // Segment sg of a tile = word (sg % 8) of block (sg / 8): K offset 16 * sg.
-  __device__ static void decode(const ScalarParams&, int, int, int sg, const uint8_t* sW, Seg& g) {
+  __device__ static void decode(const ScalarParams&, int, int, int sg, const uint8_t* sW, const uint8_t*,
+                                Seg& g) {
     const uint8_t* blk = sW + (sg >> 3) * 34;
     q2_decode_f32(q2_code_word(blk, sg & 7), g.w);
     g.s = q2_scale(blk);

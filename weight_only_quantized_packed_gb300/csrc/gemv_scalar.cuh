@@ -4,19 +4,22 @@
 // Thread map (after "spark_model/layers/ops/gemv_q2_vec.rs", doc of
 // `q2_0_gemv_vec`, and the register-tiled T=2 tier of
 // "spark_model/layers/w4a16_gemv_tiers.rs", doc of `resolve`):
-//   warps 0..7  consumers: warp w owns output rows n0 + 2w and n0 + 2w + 1
+//   warps 0..8  consumers: warp w owns output rows n0 + 2w and n0 + 2w + 1
 //               and keeps M FP32 accumulator pairs per row, so every weight
 //               word is read once for all M rows (doc of
 //               `q2_0_gemv_vec_batchm`) and every activation load serves two
 //               weight rows;
-//   warp 8      producer: streams the CTA's 16-row weight slab and the M
-//               BF16 activation rows through a STAGES-deep ring of K tiles
-//               with non-multicast bulk copies (cp.async.bulk, one lane per
-//               row, issued in parallel) and mbarriers. If the rows are not
-//               16-byte aligned, the producer warp copies with plain loads.
-// Per K tile the consumers first widen the activation tile to FP32 in shared
-// memory (double-buffered, one named barrier per tile), then stream the
-// weight segments.
+//   warp 9      producer: streams the CTA's 18-row weight slab through a
+//               STAGES-deep ring of K tiles, one 2-D tensor-map copy
+//               (cp.async.bulk.tensor) per tile (rows past N and K past the
+//               end are zero-filled). If the weight rows are not 16-byte
+//               aligned, the producer warp copies them with plain loads.
+// Activations are widened to FP32 in shared memory (XOR-swizzled, with the
+// format's per-position pre-scale). When M * K * 4 bytes fit (ARES), the
+// consumers widen all of A once, straight from global memory, while the first
+// weight tiles are in flight; afterwards each warp waits only on weight
+// tiles. Otherwise the producer also copies each tile's M BF16 activation
+// rows, and the consumers widen them tile by tile behind a named barrier.
 //
 // Per-row arithmetic (identical for every M, so a batched row equals the M = 1
 // row bit for bit): weights are decoded to exact FP32 values. For each
@@ -24,17 +27,20 @@
 // k = 8..15, even and odd k in the two halves) are added, the segment's scale
 // is folded with one FFMA2 onto the lane's accumulator pair, and at the end
 // the pair is summed and the 32 lanes reduced by a fixed xor-butterfly. The
-// order depends only on N and K, never on M.
+// order depends only on N and K, never on M or on the staging path.
 #pragma once
+#include <cuda.h>
+
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace wqp {
 
-constexpr int kWarpsC = 8;                  // consumer warps
+constexpr int kWarpsC = 9;                     // consumer warps
 constexpr int kRowsPerWarp = 2;
 constexpr int kRows = kWarpsC * kRowsPerWarp;  // output rows per CTA
 constexpr int kThreads = (kWarpsC + 1) * 32;
-static_assert(kRows + 16 <= 32, "producer lanes: one per weight row, then one per activation row");
+constexpr int kAResMaxBytes = 96 * 1024;       // resident FP32 activations, at most
 
 __device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
 
@@ -55,36 +61,61 @@ struct Seg {
   float s;
 };
 
-// Position of the 16-byte chunk j (0..3) of segment sg in the FP32 activation
-// buffer: XOR-swizzled so that the 8 lanes of a shared-memory phase, which
-// read 8 consecutive segments, hit 8 distinct bank groups.
+// Position of the 16-byte chunk j (0..3) of segment sg in an FP32 activation
+// row: XOR-swizzled so that the 8 lanes of a shared-memory phase, which read
+// 8 consecutive segments, hit 8 distinct bank groups.
 __device__ __forceinline__ int fa_chunk(int sg, int j) { return sg * 4 + (j ^ ((sg >> 1) & 3)); }
+
+// Widens 16 BF16 activations (two 16-byte words) to FP32 with the format's
+// pre-scale and stores them as segment sg of the FP32 row.
+template <class F>
+__device__ __forceinline__ void widen_segment(uint4 v0, uint4 v1, float* row, int sg) {
+  float4* r4 = reinterpret_cast<float4*>(row);
+  r4[fa_chunk(sg, 0)] = make_float4(bf16lo(v0.x) * F::prescale(0), bf16hi(v0.x) * F::prescale(1),
+                                    bf16lo(v0.y) * F::prescale(2), bf16hi(v0.y) * F::prescale(3));
+  r4[fa_chunk(sg, 1)] = make_float4(bf16lo(v0.z) * F::prescale(4), bf16hi(v0.z) * F::prescale(5),
+                                    bf16lo(v0.w) * F::prescale(6), bf16hi(v0.w) * F::prescale(7));
+  r4[fa_chunk(sg, 2)] = make_float4(bf16lo(v1.x) * F::prescale(8), bf16hi(v1.x) * F::prescale(9),
+                                    bf16lo(v1.y) * F::prescale(10), bf16hi(v1.y) * F::prescale(11));
+  r4[fa_chunk(sg, 3)] = make_float4(bf16lo(v1.z) * F::prescale(12), bf16hi(v1.z) * F::prescale(13),
+                                    bf16lo(v1.w) * F::prescale(14), bf16hi(v1.w) * F::prescale(15));
+}
 
 // Format traits interface (gemv_q2.cu, gemv_w4.cu, gemv_w8.cu):
 //   kTK                 K elements per ring stage (multiple of 128)
-//   kWRow               weight bytes of one row per stage
-//   bulk_ok(K)          host: bulk-copy fast path allowed for this K
-//   row_tile_bytes(tg)  bytes of one row's tile with tg groups
-//   issue_row_bulk(...) producer lane: bulk copies of one row's tile
+//   kWRow, kW2Row       weight bytes of one row per stage in the first and
+//                       (W4 scales) second block of the stage
+//   bulk_ok(K)          host: tensor-map path allowed for this K
+//   make_maps(...)      host: tensor maps of the weight block(s)
+//   issue_tile(...)     producer lane: tensor-map copies of one K tile
 //   copy_row_plain(...) producer warp: plain-load copy of one row's tile
 //   prescale(p)         factor applied to a[k] when widened (p = k % 16)
 //   decode(...)         consumer: one segment of one row -> Seg
-template <class F, int M>
+template <class F, int M, bool ARES>
 struct ScalarCfg {
-  static constexpr int kStages = (M <= 4) ? 6 : (M <= 8 ? 4 : 2);
-  static constexpr int kWStage = kRows * F::kWRow;
-  static constexpr int kAStage = M * F::kTK * 2;
+  static constexpr int kStages = ARES ? (M <= 2 ? 6 : 4) : ((M <= 4) ? 4 : (M <= 8 ? 3 : 2));
+  static constexpr bool kFADouble = !ARES && (M <= 4);    // double-buffered per-tile FP32 A
+  static constexpr int kW2Off = kRows * F::kWRow;
+  static constexpr int kWStage = (kRows * (F::kWRow + F::kW2Row) + 127) / 128 * 128;
+  static constexpr int kAW = F::kTK < 512 ? F::kTK : 512;   // K per activation box
+  static constexpr int kAStage = ARES ? 0 : M * F::kTK * 2;
   static constexpr int kStageBytes = ((kWStage + kAStage) + 127) / 128 * 128;
-  static constexpr int kFABytes = M * F::kTK * 4;           // one FP32 activation buffer
-  static constexpr int kSmem = kStages * kStageBytes + 2 * kFABytes;
-  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static constexpr int kFABytes = ARES ? 0 : M * F::kTK * 4;  // one per-tile FP32 buffer
+  static constexpr int kSmemFixed = kStages * kStageBytes + (kFADouble ? 2 : 1) * kFABytes;
+  static constexpr int kSmemMax = kSmemFixed + (ARES ? kAResMaxBytes : 0);
+  static constexpr int kMinBlocks = (M <= 8) ? 2 : 1;
+  static_assert(kSmemMax <= 227 * 1024, "shared memory budget");
+  static_assert(F::kW2Row == 0 || (kRows * F::kWRow) % 128 == 0, "second weight block alignment");
 };
 
-template <class F, int M, bool BULK>
-__global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
-  using Cfg = ScalarCfg<F, M>;
+template <class F, int M, bool BULK, bool ARES>
+__global__ void __launch_bounds__(kThreads, (ScalarCfg<F, M, ARES>::kMinBlocks))
+    gemv_scalar_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
+                       const __grid_constant__ CUtensorMap tmA, ScalarParams p) {
+  using Cfg = ScalarCfg<F, M, ARES>;
   constexpr int kStages = Cfg::kStages;
   constexpr int TK = F::kTK;
+  constexpr int kSegT = TK / 16;                 // segments per row per full tile
 
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -99,6 +130,7 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
   constexpr int kGT = TK / 128;                  // groups per full tile
   const int tiles = (G + kGT - 1) / kGT;
   float* fA = reinterpret_cast<float*>(smem + kStages * Cfg::kStageBytes);
+  const int ldfa = ARES ? K : TK;                // FP32 activation row pitch (floats)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -113,6 +145,10 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
   if (warp == kWarpsC) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+      if (BULK) { tc::prefetch_tmap(&tmW); if (F::kW2Row) tc::prefetch_tmap(&tmW2); }
+      if (!ARES) tc::prefetch_tmap(&tmA);
+    }
     int issued = 0;
     for (int t = 0; t < tiles; ++t) {
       const int s = t % kStages;
@@ -125,26 +161,24 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
       const int tg = min(kGT, G - t * kGT);      // groups in this tile
       uint8_t* sW = smem + s * Cfg::kStageBytes;
       uint8_t* sAs = sW + Cfg::kWStage;
-      const uint32_t abytes = static_cast<uint32_t>(tg) * 128 * 2;
       const uint32_t fb = smem_u32(&full_bar[s]);
       if (!BULK) {
-        for (int r = 0; r < rows; ++r) F::copy_row_plain(p, n0 + r, t, tg, sW + r * F::kWRow, lane);
+        for (int r = 0; r < rows; ++r)
+          F::copy_row_plain(p, n0 + r, t, tg, sW + r * F::kWRow, sW + Cfg::kW2Off + r * F::kW2Row, lane);
         __threadfence_block();
         __syncwarp();
       }
-      // One lane posts the stage's byte count, then the copies are issued in
-      // parallel: lane r < 16 copies weight row r, lane 16 + m activation row m.
       if (lane == 0) {
-        const uint32_t tx = (BULK ? F::row_tile_bytes(tg) * rows : 0u) + abytes * M;
+        // Full boxes always land (out-of-range rows and K read as zero).
+        const uint32_t tx = (BULK ? kRows * (F::kWRow + F::kW2Row) : 0u) + Cfg::kAStage;
         mbar_arrive_expect_tx(fb, tx);
-      }
-      __syncwarp();
-      if (BULK && lane < rows)
-        F::issue_row_bulk(p, n0 + lane, t, tg, smem_u32(sW + lane * F::kWRow), fb, pol);
-      if (lane >= kRows && lane - kRows < M) {
-        const int m = lane - kRows;
-        if (t == 0) pdl_wait();            // activations may come from the previous kernel
-        bulk_g2s(smem_u32(sAs + m * TK * 2), p.A + static_cast<size_t>(m) * p.lda + t * TK, abytes, fb);
+        if (BULK) F::issue_tile(&tmW, &tmW2, smem_u32(sW), smem_u32(sW + Cfg::kW2Off), t, n0, fb, pol);
+        if (!ARES) {
+          if (t == 0) pdl_wait();          // activations may come from the previous kernel
+#pragma unroll
+          for (int bx = 0; bx < TK / Cfg::kAW; ++bx)
+            tc::tma_load_2d(smem_u32(sAs + bx * M * Cfg::kAW * 2), &tmA, (t * TK + bx * Cfg::kAW) / 2, 0, fb);
+        }
       }
       issued = t + 1;
     }
@@ -156,6 +190,21 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
   }
 
   // -------------------------------------------------------------- consumers
+  constexpr int kCT = kWarpsC * 32;              // consumer threads
+  if (ARES) {
+    // Widen all of A once, straight from global memory (it may come from the
+    // previous kernel, hence the dependency wait first).
+    pdl_wait();
+    const int segK = K / 16;
+    for (int u = threadIdx.x; u < M * segK; u += kCT) {
+      const int m = u / segK;
+      const int sg = u - m * segK;
+      const uint4* src = reinterpret_cast<const uint4*>(p.A + static_cast<size_t>(m) * p.lda + sg * 16);
+      widen_segment<F>(__ldg(src), __ldg(src + 1), fA + m * ldfa, sg);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory");
+  }
+
   float2 acc[kRowsPerWarp][M];
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r)
@@ -167,8 +216,7 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
     const int s = t % kStages;
     // Every lane waits (acquire) and the warp agrees on the outcome, so a
     // timeout never splits the warp. After a timeout the loop keeps running
-    // the named barrier (no compute) so the other consumer warps never wait
-    // on it for ever.
+    // the named barriers (no compute) so other warps never wait for ever.
     if (ok) {
       const bool got = mbar_wait(smem_u32(&full_bar[s]), (t / kStages) & 1, p.err);
       if (!__all_sync(0xFFFFFFFFu, got)) ok = false;
@@ -176,47 +224,52 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
     const int tg = min(kGT, G - t * kGT);
     const int segs = tg * 8;
     const uint8_t* sW = smem + s * Cfg::kStageBytes;
-    const uint16_t* sAs = reinterpret_cast<const uint16_t*>(sW + Cfg::kWStage);
-    float* fAt = fA + (t & 1) * (M * TK);
-    // Widen the activation tile to FP32, one 16-element segment per unit,
-    // applying the format's per-position pre-scale (a power of two).
-    if (ok) {
-      const int units = M * segs;
-      for (int u = threadIdx.x; u < units; u += kWarpsC * 32) {
-        const int m = u / segs;
-        const int sg = u - m * segs;
-        const uint4* src = reinterpret_cast<const uint4*>(sAs + m * TK + sg * 16);
-        const uint4 v0 = src[0], v1 = src[1];
-        float4* row = reinterpret_cast<float4*>(fAt + m * TK);
-        row[fa_chunk(sg, 0)] = make_float4(bf16lo(v0.x) * F::prescale(0), bf16hi(v0.x) * F::prescale(1),
-                                           bf16lo(v0.y) * F::prescale(2), bf16hi(v0.y) * F::prescale(3));
-        row[fa_chunk(sg, 1)] = make_float4(bf16lo(v0.z) * F::prescale(4), bf16hi(v0.z) * F::prescale(5),
-                                           bf16lo(v0.w) * F::prescale(6), bf16hi(v0.w) * F::prescale(7));
-        row[fa_chunk(sg, 2)] = make_float4(bf16lo(v1.x) * F::prescale(8), bf16hi(v1.x) * F::prescale(9),
-                                           bf16lo(v1.y) * F::prescale(10), bf16hi(v1.y) * F::prescale(11));
-        row[fa_chunk(sg, 3)] = make_float4(bf16lo(v1.z) * F::prescale(12), bf16hi(v1.z) * F::prescale(13),
-                                           bf16lo(v1.w) * F::prescale(14), bf16hi(v1.w) * F::prescale(15));
+    const float* fAt;
+    int sg0;                                      // segment offset of this tile in fAt
+    if (ARES) {
+      fAt = fA;
+      sg0 = t * kSegT;
+    } else {
+      const uint16_t* sAs = reinterpret_cast<const uint16_t*>(sW + Cfg::kWStage);
+      float* fAw = fA + (Cfg::kFADouble ? (t & 1) * (M * TK) : 0);
+      fAt = fAw;
+      sg0 = 0;
+      // With a single FP32 buffer, wait until every warp is done with the
+      // previous tile before overwriting it.
+      if (!Cfg::kFADouble && t > 0) asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory");
+      if (ok) {
+        for (int u = threadIdx.x; u < M * segs; u += kCT) {
+          const int m = u / segs;
+          const int sg = u - m * segs;
+          // Activation tile layout: boxes of kAW K, each [M rows x kAW].
+          const int k0 = sg * 16;
+          const uint4* src = reinterpret_cast<const uint4*>(
+              sAs + (k0 / Cfg::kAW) * (M * Cfg::kAW) + m * Cfg::kAW + (k0 % Cfg::kAW));
+          widen_segment<F>(src[0], src[1], fAw + m * ldfa, sg);
+        }
       }
+      asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory");
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kWarpsC * 32) : "memory");
     if (ok) {
       for (int sg = lane; sg < segs; sg += 32) {
         Seg g[kRowsPerWarp];
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) {
           if (r0 + r < rows) {
-            F::decode(p, n0 + r0 + r, t, sg, sW + (r0 + r) * F::kWRow, g[r]);
+            F::decode(p, n0 + r0 + r, t, sg, sW + (r0 + r) * F::kWRow,
+                      sW + Cfg::kW2Off + (r0 + r) * F::kW2Row, g[r]);
           } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) g[r].w[i] = make_float2(0.f, 0.f);
             g[r].s = 0.f;
           }
         }
+        const int sa = sg0 + sg;
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          const float4* row = reinterpret_cast<const float4*>(fAt + m * TK);
-          const float4 q0 = row[fa_chunk(sg, 0)], q1 = row[fa_chunk(sg, 1)];
-          const float4 q2 = row[fa_chunk(sg, 2)], q3 = row[fa_chunk(sg, 3)];
+          const float4* row = reinterpret_cast<const float4*>(fAt + m * ldfa);
+          const float4 q0 = row[fa_chunk(sa, 0)], q1 = row[fa_chunk(sa, 1)];
+          const float4 q2 = row[fa_chunk(sa, 2)], q3 = row[fa_chunk(sa, 3)];
           const float2 a[8] = {make_float2(q0.x, q0.y), make_float2(q0.z, q0.w),
                                make_float2(q1.x, q1.y), make_float2(q1.z, q1.w),
                                make_float2(q2.x, q2.y), make_float2(q2.z, q2.w),
@@ -251,16 +304,27 @@ __global__ void __launch_bounds__(kThreads) gemv_scalar_kernel(ScalarParams p) {
   }
 }
 
-template <class F, int M, bool BULK>
+// Host: tensor map of the activation rows, viewed as u32 pairs of BF16.
+cudaError_t make_act_map(CUtensorMap* m, const GemvArgs& a, int box_k);
+// Host: 2-D tensor map (rows x bytes) helper shared by the format traits.
+cudaError_t make_rows_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+
+template <class F, int M, bool BULK, bool ARES>
 cudaError_t launch_scalar_m(const GemvArgs& a, cudaStream_t s) {
-  auto kern = gemv_scalar_kernel<F, M, BULK>;
-  constexpr int smem = ScalarCfg<F, M>::kSmem;
+  using Cfg = ScalarCfg<F, M, ARES>;
+  auto kern = gemv_scalar_kernel<F, M, BULK, ARES>;
   static bool attr_set = false;  // idempotent; racing writers set the same value
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemMax);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  const int smem = Cfg::kSmemFixed + (ARES ? M * a.K * 4 : 0);
+  CUtensorMap mw = {}, mw2 = {}, ma = {};
+  cudaError_t e = cudaSuccess;
+  if (!ARES && (e = make_act_map(&ma, a, Cfg::kAW)) != cudaSuccess) return e;
+  if (BULK && (e = F::make_maps(a, &mw, &mw2)) != cudaSuccess) return e;
   ScalarParams p;
   p.A = static_cast<const uint16_t*>(a.A);
   p.W = static_cast<const uint8_t*>(a.W);
@@ -273,28 +337,35 @@ cudaError_t launch_scalar_m(const GemvArgs& a, cudaStream_t s) {
   p.gscale = a.gscale;
   p.err = a.err;
   dim3 grid((a.N + kRows - 1) / kRows);
-  return launch(kern, grid, dim3(kThreads), smem, s, a.pdl, p);
+  return launch(kern, grid, dim3(kThreads), smem, s, a.pdl, mw, mw2, ma, p);
+}
+
+template <class F, int M, bool BULK>
+cudaError_t launch_scalar_m2(const GemvArgs& a, cudaStream_t s) {
+  // Keep A resident when it fits; the per-tile path otherwise.
+  if (static_cast<long long>(M) * a.K * 4 <= kAResMaxBytes) return launch_scalar_m<F, M, BULK, true>(a, s);
+  return launch_scalar_m<F, M, BULK, false>(a, s);
 }
 
 template <class F, bool BULK>
 cudaError_t launch_scalar_dispatch(const GemvArgs& a, cudaStream_t s) {
   switch (a.M) {
-    case 1: return launch_scalar_m<F, 1, BULK>(a, s);
-    case 2: return launch_scalar_m<F, 2, BULK>(a, s);
-    case 3: return launch_scalar_m<F, 3, BULK>(a, s);
-    case 4: return launch_scalar_m<F, 4, BULK>(a, s);
-    case 5: return launch_scalar_m<F, 5, BULK>(a, s);
-    case 6: return launch_scalar_m<F, 6, BULK>(a, s);
-    case 7: return launch_scalar_m<F, 7, BULK>(a, s);
-    case 8: return launch_scalar_m<F, 8, BULK>(a, s);
-    case 9: return launch_scalar_m<F, 9, BULK>(a, s);
-    case 10: return launch_scalar_m<F, 10, BULK>(a, s);
-    case 11: return launch_scalar_m<F, 11, BULK>(a, s);
-    case 12: return launch_scalar_m<F, 12, BULK>(a, s);
-    case 13: return launch_scalar_m<F, 13, BULK>(a, s);
-    case 14: return launch_scalar_m<F, 14, BULK>(a, s);
-    case 15: return launch_scalar_m<F, 15, BULK>(a, s);
-    case 16: return launch_scalar_m<F, 16, BULK>(a, s);
+    case 1: return launch_scalar_m2<F, 1, BULK>(a, s);
+    case 2: return launch_scalar_m2<F, 2, BULK>(a, s);
+    case 3: return launch_scalar_m2<F, 3, BULK>(a, s);
+    case 4: return launch_scalar_m2<F, 4, BULK>(a, s);
+    case 5: return launch_scalar_m2<F, 5, BULK>(a, s);
+    case 6: return launch_scalar_m2<F, 6, BULK>(a, s);
+    case 7: return launch_scalar_m2<F, 7, BULK>(a, s);
+    case 8: return launch_scalar_m2<F, 8, BULK>(a, s);
+    case 9: return launch_scalar_m2<F, 9, BULK>(a, s);
+    case 10: return launch_scalar_m2<F, 10, BULK>(a, s);
+    case 11: return launch_scalar_m2<F, 11, BULK>(a, s);
+    case 12: return launch_scalar_m2<F, 12, BULK>(a, s);
+    case 13: return launch_scalar_m2<F, 13, BULK>(a, s);
+    case 14: return launch_scalar_m2<F, 14, BULK>(a, s);
+    case 15: return launch_scalar_m2<F, 15, BULK>(a, s);
+    case 16: return launch_scalar_m2<F, 16, BULK>(a, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -8,38 +8,42 @@ namespace wqp {
 
 struct W4Fmt {
   static constexpr int kTK = 512;                  // 4 groups per stage
-  static constexpr int kWRow = 256 + 32;           // codes + E4M3 scales of 512 K
-  // Scale rows start at n * K/16: 16-byte aligned for every n iff K % 256 == 0
-  // (which also makes every tile's 8 * tg scale bytes a multiple of 16).
+  static constexpr int kWRow = 256;                // code bytes of 512 K
+  static constexpr int kW2Row = 32;                // E4M3 scale bytes of 512 K
+  // Scale rows are K/16 bytes: a multiple of 16 iff K % 256 == 0.
   static bool bulk_ok(int K) { return K % 256 == 0; }
-  __device__ static uint32_t row_tile_bytes(int tg) { return 64u * tg + 8u * tg; }
-  __device__ static void issue_row_bulk(const ScalarParams& p, int n, int t, int tg, uint32_t dst,
-                                        uint32_t bar, uint64_t pol) {
-    const size_t K = static_cast<size_t>(p.K);
-    bulk_g2s_stream(dst, p.W + n * (K / 2) + 256 * t, 64u * tg, bar, pol);
-    bulk_g2s_stream(dst + 256, static_cast<const uint8_t*>(p.scales) + n * (K / 16) + 32 * t,
-                    8u * tg, bar, pol);
+  static cudaError_t make_maps(const GemvArgs& a, CUtensorMap* mw, CUtensorMap* ms) {
+    const uint64_t K = static_cast<uint64_t>(a.K);
+    cudaError_t e = make_rows_map(mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, K / 8, a.N, K / 2, kWRow / 4, kRows);
+    if (e != cudaSuccess) return e;
+    return make_rows_map(ms, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.scales, K / 64, a.N, K / 16, kW2Row / 4, kRows);
+  }
+  __device__ static void issue_tile(const CUtensorMap* mw, const CUtensorMap* ms, uint32_t dst,
+                                    uint32_t dst2, int t, int n0, uint32_t bar, uint64_t pol) {
+    tc::tma_load_2d_hint(dst, mw, t * (kWRow / 4), n0, bar, pol);
+    tc::tma_load_2d_hint(dst2, ms, t * (kW2Row / 4), n0, bar, pol);
   }
   __device__ static void copy_row_plain(const ScalarParams& p, int n, int t, int tg, uint8_t* dst,
-                                        int lane) {
+                                        uint8_t* dst2, int lane) {
     const size_t K = static_cast<size_t>(p.K);
     const uint32_t* c = reinterpret_cast<const uint32_t*>(p.W + n * (K / 2) + 256 * t);
     for (int i = lane; i < 16 * tg; i += 32) reinterpret_cast<uint32_t*>(dst)[i] = __ldg(c + i);
-    const uint32_t* sc =
-        reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(p.scales) + n * (K / 16) + 32 * t);
-    for (int i = lane; i < 2 * tg; i += 32) reinterpret_cast<uint32_t*>(dst + 256)[i] = __ldg(sc + i);
+    const uint16_t* sc =
+        reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(p.scales) + n * (K / 16) + 32 * t);
+    for (int i = lane; i < 4 * tg; i += 32) reinterpret_cast<uint16_t*>(dst2)[i] = __ldg(sc + i);
   }
   __device__ static constexpr float prescale(int) { return 1.0f; }
   // Segment sg = K elements [16 sg, 16 sg + 16) of the tile: 8 code bytes and
   // the one E4M3 scale of that 16-group.
-  __device__ static void decode(const ScalarParams& p, int, int, int sg, const uint8_t* sW, Seg& g) {
+  __device__ static void decode(const ScalarParams& p, int, int, int sg, const uint8_t* sW,
+                                const uint8_t* sW2, Seg& g) {
     const uint2 c = *reinterpret_cast<const uint2*>(sW + 8 * sg);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       g.w[i] = f16x2_to_float2(e2m1x2_to_f16x2((c.x >> (8 * i)) & 0xFFu));
       g.w[4 + i] = f16x2_to_float2(e2m1x2_to_f16x2((c.y >> (8 * i)) & 0xFFu));
     }
-    g.s = e4m3_to_f32(sW[256 + sg]) * p.gscale;
+    g.s = e4m3_to_f32(sW2[sg]) * p.gscale;
   }
 };
 

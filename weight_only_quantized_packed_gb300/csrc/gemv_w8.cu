@@ -12,19 +12,24 @@ namespace wqp {
 struct W8Fmt {
   static constexpr int kTK = 512;
   static constexpr int kWRow = 512;
-  static bool bulk_ok(int) { return true; }   // rows start at n * K, K % 128 == 0
-  __device__ static uint32_t row_tile_bytes(int tg) { return 128u * tg; }
-  __device__ static void issue_row_bulk(const ScalarParams& p, int n, int t, int tg, uint32_t dst,
-                                        uint32_t bar, uint64_t pol) {
-    bulk_g2s_stream(dst, p.W + static_cast<size_t>(n) * p.K + 512 * t, 128u * tg, bar, pol);
+  static constexpr int kW2Row = 0;
+  static bool bulk_ok(int) { return true; }   // rows are K bytes, K % 128 == 0
+  static cudaError_t make_maps(const GemvArgs& a, CUtensorMap* mw, CUtensorMap*) {
+    const uint64_t K = static_cast<uint64_t>(a.K);
+    return make_rows_map(mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, K / 4, a.N, K, kWRow / 4, kRows);
   }
-  __device__ static void copy_row_plain(const ScalarParams& p, int n, int t, int tg, uint8_t* dst,
+  __device__ static void issue_tile(const CUtensorMap* mw, const CUtensorMap*, uint32_t dst, uint32_t,
+                                    int t, int n0, uint32_t bar, uint64_t pol) {
+    tc::tma_load_2d_hint(dst, mw, t * (kWRow / 4), n0, bar, pol);
+  }
+  __device__ static void copy_row_plain(const ScalarParams& p, int n, int t, int tg, uint8_t* dst, uint8_t*,
                                         int lane) {
     const uint4* c = reinterpret_cast<const uint4*>(p.W + static_cast<size_t>(n) * p.K + 512 * t);
     for (int i = lane; i < 8 * tg; i += 32) reinterpret_cast<uint4*>(dst)[i] = __ldg(c + i);
   }
   __device__ static constexpr float prescale(int) { return 1.0f; }
-  __device__ static void decode(const ScalarParams& p, int n, int t, int sg, const uint8_t* sW, Seg& g) {
+  __device__ static void decode(const ScalarParams& p, int n, int t, int sg, const uint8_t* sW, const uint8_t*,
+                                Seg& g) {
     const uint4 c = *reinterpret_cast<const uint4*>(sW + 16 * sg);
     const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll

@@ -2,6 +2,7 @@
 // translation units. Not installed; the public surface is include/wqp.h.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace wqp {
@@ -41,6 +42,12 @@ cudaError_t launch_q2_gemm_tc(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_q2_dequant(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_w4a16_dequant(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_w8a16_dequant(const DequantArgs& a, cudaStream_t s);
+
+// 2-D tensor map (tmap.cu): inner extent in elements, row pitch in bytes,
+// box of box_inner x box_outer elements, no interleave, zero out-of-range fill.
+cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMapSwizzle sw);
 
 // Launch helper: programmatic stream serialization when pdl is set.
 template <typename Kern, typename... Args>

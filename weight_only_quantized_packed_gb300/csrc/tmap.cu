@@ -1,0 +1,55 @@
+// Host-side tensor-map encoding (cuTensorMapEncodeTiled, reached through the
+// runtime's driver entry point so no driver library is linked).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemv_scalar.cuh"
+#include "internal.h"
+
+namespace wqp {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_act_map(CUtensorMap* m, const GemvArgs& a, int box_k) {
+  // BF16 pairs as u32: K/2 columns, M rows, pitch lda * 2 bytes.
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.A, static_cast<uint64_t>(a.K / 2),
+                     static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda) * 2,
+                     static_cast<uint32_t>(box_k / 2), static_cast<uint32_t>(a.M), CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+cudaError_t make_rows_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+  return make_map_2d(m, dt, base, inner, rows, row_bytes, box_inner, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+}  // namespace wqp
