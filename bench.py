@@ -191,7 +191,9 @@ class Workload:
         self.i += 1
         A = self.A[M] if A is None else A
         C = self.C[M] if C is None else C
-        if self.fmt == "q2":
+        if self.fmt == "q2" and self.tc:
+            wqp.q2_gemm_tc(A, self.W[j], self.N, self.K, out=C)
+        elif self.fmt == "q2":
             wqp.q2_gemv(A, self.W[j], self.N, self.K, out=C)
         elif self.fmt == "w4":
             wqp.w4a16_gemv(A, self.W[j], self.S[j], self.N, self.K, out=C)
@@ -230,6 +232,7 @@ def sweep(l2, peak):
     specs = [
         ("q2_gemv N=256 K=512", "q2", 256, 512, (1,), False, 0),
         ("q2_gemv N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), False, 1),
+        ("q2_gemm_tc N=5120 K=5120", "q2", 5120, 5120, (1, 8, 16), True, 1),
         ("w4a16_gemv N=5120 K=5120", "w4", 5120, 5120, tuple(range(1, 9)), False, 2),
         ("w8a16_gemm N=17408 K=5120", "w8", 17408, 5120, (1, 4, 8, 16), False, 3),
         ("w8a16_gemm N=5120 K=17408", "w8", 5120, 17408, (1, 4, 8, 16), False, 3),
@@ -491,6 +494,27 @@ def reference_arm(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def profile_case(case, launches, pdl):
+    """A fixed number of launches of one call shape, for ncu captures."""
+    import torch
+
+    import weight_only_quantized_packed_gb300 as wqp
+
+    parts = case.split(":")
+    fmt, M, N, K = parts[0], int(parts[1]), int(parts[2]), int(parts[3])
+    tc = len(parts) > 4 and parts[4] == "tc"
+    wqp.set_pdl(bool(pdl))
+    # About 192 MiB of cycled weights: past L2 (129 MB), well under 1 GiB on the device.
+    w = Workload(fmt, N, K, (M,), 64 << 20, 9, tc=tc, cap_bytes=1 << 30)
+    for _ in range(launches):
+        w.call(M)
+    torch.cuda.synchronize()
+    err = wqp.get_device_error()
+    print(json.dumps({"case": case, "launches": launches, "buffers": w.nbuf, "device_error": err}))
+    if err:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -501,7 +525,14 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", default=None,
+                    help="profiling mode: run --launches calls of one shape, fmt:M:N:K[:tc] "
+                         "(fmt q2|w4|w8), weights cycled past L2; prints one status line")
+    ap.add_argument("--launches", type=int, default=6)
     args = ap.parse_args()
+    if args.case:
+        profile_case(args.case, args.launches, args.pdl)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
