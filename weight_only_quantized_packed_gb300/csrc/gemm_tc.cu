@@ -10,157 +10,273 @@
 //
 // Swap-AB: the 128 weight rows of a tile are the MMA's M side, and the M <= 16
 // activation rows, zero-padded to 16, are its N side:
-//   D[n, m] = sum_k W[n, k] * A[m, k]   (tcgen05.mma kind::f16, M=128 N=16 K=16)
-// Every E4M3 value and every Q2_0 code - 1 is exactly representable in BF16,
-// so the products are exact. The tensor core reduces each 16-K step in its
-// own order, so the result is not bit-identical to the scalar kernels. Each
-// output row still depends only on its own activation row.
+//   D[n, m] = sum_k W[n, k] * A[m, k]   (tcgen05.mma kind::f16, BF16 in, FP32
+//                                        accumulate, M=128 N=16 K=16)
+// The weight operand lives in tensor memory: converter warps decode the packed
+// bytes in registers and write BF16 pairs with tcgen05.st (one weight row per
+// TMEM lane, two K elements per 32-bit column); the MMA reads A from TMEM and
+// the activation operand B from shared memory. No operand round-trips through
+// shared memory.
 //
-// One CTA = one 128-row tile x a contiguous range of 128-K groups. Roles:
-//   warp 20     TMA: raw weight tiles (FP8: [128 rows x 128 B] with 128-byte
-//               swizzle; Q2_0: [128 rows x 272 B] = 8 groups) and activation
-//               tiles [16 rows x 64 K] x 2 (128-byte swizzle, rows past M
-//               zero-filled), through mbarrier rings;
-//   warps 0..15 decode one row and a quarter group (32 K) per thread into the
-//               K-major BF16 operand tile (128-byte swizzle, like the
-//               activations);
-//   warp 21     allocates TMEM and issues the 8 MMAs of each group into its
-//               own 16-column accumulator slot, then commits;
-//   warps 16..19 fold each group: tcgen05.ld of the slot (lane = weight row,
-//               column = activation row), acc[m] += s * D[m] in FP32.
-// When N is small, K is split over a thread-block cluster of up to 8 CTAs.
-// The partial sums are added in rank order through distributed shared memory
-// (deterministic, no global scratch).
+// Encodings (every product is exact in FP32):
+//  * FP8: each E4M3 value is a BF16 value; B is the activation tile as loaded.
+//  * Q2_0: the two codes (c_j, c_{j+8}) of a 16-code word sit at bits (2j,
+//    2j+16). Masking them in place (one LOP3 per pair) gives two BF16
+//    subnormals c * 4^(j mod 4) * 2^-133 (exact: the field stays below the
+//    first normal binade, where the BF16 encoding is linear). The matching
+//    activations are pre-scaled by 2^(64 - 2 (j mod 4)) (exact), so each
+//    product is c * a * 2^-69. Per 128-K group g and activation row m,
+//    sum_k (c_k - 1) a_k = 2^69 * D[n, m] - S[m, g] with S = sum_k a_k, and the
+//    fp16 scale d folds in FP32: acc += d * (2^69 D - S).
+//    The MMA's K order inside a 16-K step is the code-pair order
+//    (16i + c', 16i + c' + 8) for column c' = 0..7; the activation operand is
+//    written in that same order.
+// The tensor core reduces each 16-K step in its own order, so results are not
+// bit-identical to the scalar kernels; each output element still depends only
+// on its own weight row and activation row.
+//
+// One CTA = one tile of weight rows x a contiguous range of 128-K groups (a
+// multiple of the raw stage). Warps:
+//   0..7   converters, in two sets (group parity = warp / 4), TMEM lane
+//          quarter = warp % 4; each thread converts one weight row of one
+//          group (64 columns);
+//   8..11  epilogue: per group, tcgen05.ld of the group's accumulator slot
+//          (lane = weight row, column = activation row) and the FP32 fold;
+//   12     TMA: lane 0 raw weight stages, lane 1 activation tiles;
+//   13     MMA: allocates TMEM; per group one wait, then the elected lane
+//          issues the 8 MMAs into the group's accumulator slot and commits
+//          once ("MMA of group j done");
+//   14..15 activation operand hand-off (alternate groups): Q2_0 tiles are
+//          prepared in place on the tile the TMA loaded; FP8 tiles are used
+//          as loaded.
+// The MMA warp waits on a single barrier per group, "group j may start",
+// which completes after nine arrivals: the four converter warps of the set,
+// the activation operand (its hand-off warp) and
+// the four epilogue warps releasing the accumulator slot (pre-armed for the
+// first NACC groups). A warp that issues MMAs stalls at its next
+// shared-memory access until the tensor core has taken them, so the MMA
+// warp does nothing else.
+// Q2_0 tiles are 124 weight rows: the last lane of each 32-lane quarter of
+// TMEM (lanes 31, 63, 95, 127) holds a row of all-ones codes, whose
+// accumulator is 2^-69 * sum_k a_k, the group sum the fold needs, computed by
+// the same MMAs and read by each epilogue warp from its own lane 31.
+// When N is small, K is split over a thread-block cluster of up to 8 CTAs;
+// the partial sums are added in rank order through distributed shared memory
+// (deterministic, no global scratch). A kernel that allocates tensor memory
+// runs one CTA per SM, so a CTA takes all 512 TMEM columns and deep rings.
 #include "decode.cuh"
 #include "tc.cuh"
 
 namespace wqp {
 namespace tc {
 
-constexpr int BM = 128;            // weight rows per tile (MMA M)
+constexpr int BM = 128;            // TMEM lanes = MMA M
 constexpr int BN = 16;             // activation rows (MMA N)
 constexpr int GK = 128;            // K per group = scale granularity
-constexpr int kConvWarps = 16;     // converters: row quarter = warp % 4, K quarter = warp / 4
-constexpr int kEpiWarp0 = 16;      // epilogue warps 16..19 (TMEM lane quarter = warp % 4)
-constexpr int kTmaWarp = 20;
-constexpr int kMmaWarp = 21;
-constexpr int kThreads = 22 * 32;
-constexpr int SA = 8;              // activation stages (prefetched independently)
-constexpr int NACC = 4;            // TMEM accumulator slots
-constexpr int NSCL = 8;            // row-scale ring (Q2_0 d), deeper than SO + NACC
-constexpr uint32_t kTmemCols = 64; // NACC * 16, rounded to a power of two >= 32
-constexpr int kOpBytes = BM * GK * 2;      // 32 KB
-constexpr int kActBytes = BN * GK * 2;     // 4 KB
+constexpr int kEpiWarp0 = 8;       // epilogue warps 8..11
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kPrepWarp0 = 14;     // activation hand-off warps 14..15
+constexpr int kPrepWarps = 2;
+constexpr int kThreads = 16 * 32;
+constexpr int SO = 6;              // TMEM operand stages, one group (64 columns) each
+constexpr int NACC = 8;            // TMEM accumulator slots, 16 columns each
+constexpr uint32_t kAccCol = SO * 64;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kAccCol + NACC * 16 <= kTmemCols, "TMEM budget");
+constexpr int SB = 8;              // activation operand stages
+constexpr int ND = 16;             // "MMA of group j done" and "group j may start" rings
+constexpr int kGoCount = 4 + 1 + 4;   // converter warps + operand + epilogue warps
+constexpr int NSC = 16;            // per-group row-scale ring (converters -> epilogue)
+
+// Ring depth: a scale slot of group j is rewritten after the MMA of group
+// j - SO completed; that MMA was issued after the epilogue released group
+// j - SO - NACC and had read its scale. A waiter on "MMA of
+// group g done" never lags the MMA by ND groups (the MMA cannot pass the
+// epilogue by more than NACC; every other waiter runs ahead of it), so the
+// parities never alias.
+static_assert(NSC >= SO + NACC, "scale ring must outlive the pipeline");
+static_assert(ND >= SB && ND >= SO && ND > NACC, "done ring depth");
+// "Group j may start" slot j % ND receives arrivals for group j only after the
+// MMA of group j - ND was issued: converters wait for MMA j - SO, the operand
+// producer for MMA j - SB, the epilogue arrives after MMA j - NACC completed.
+constexpr int kBBytes = BN * GK * 2;   // 4 KB: two [16 rows x 64 K] boxes, 128-byte swizzle
 
 struct TcParams {
   const float* scales;     // FP8: [ceil(N/128), K/128]; Q2_0: unused
   uint16_t* C;
   int M, N, K, ldc;
   int splits;              // CTAs per tile (cluster size)
-  int stages;              // raw stages per tile (K / (128 * GPR))
+  int stages;              // raw stages per tile
   unsigned* err;
 };
 
-// Operand layout: a group's 128 rows x 128 K BF16 tile is two K-major blocks
-// of 64 K, each [128 rows x 128 B] with the 128-byte swizzle (16-byte chunk c
-// of row r stored at chunk c ^ (r % 8); 8-row atoms of 1024 B). cc is the
-// 8-K chunk index within the group (0..15).
-__device__ __forceinline__ uint8_t* op_chunk(uint8_t* op, int r, int cc) {
-  return op + (cc >> 3) * (BM * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // ------------------------------------------------------------------ formats
-// FP8 E4M3: one group per raw stage, [128 rows x 128 B], 128-byte swizzle.
+// FP8 E4M3: one group per raw stage, [128 rows x 128 B], 128-byte swizzle
+// (16-byte chunk c of row r at chunk c ^ (r % 8)).
 struct Fp8Tc {
+  static constexpr int kRows = 128;              // weight rows per tile
   static constexpr int kGPR = 1;
-  static constexpr int kSR = 4;
-  static constexpr int kSO = 3;
-  static constexpr int kRawBytes = BM * GK;
-  static constexpr bool kRowScale = false;
+  static constexpr int kSR = 8;
+  static constexpr int kRawBytes = BM * GK;      // stage stride
+  static constexpr int kBoxBytes = kRows * GK;   // bytes one stage load delivers
+  static constexpr bool kQ2 = false;
+  static constexpr int kRawEmptyCount = 4;       // one converter set per stage
   __device__ static void issue_raw(const CUtensorMap* m, uint32_t dst, int g0, int n0, uint32_t bar,
                                    uint64_t pol) {
     tma_load_2d_hint(dst, m, g0 * GK, n0, bar, pol);
   }
-  // Row r, K quarter kq (32 K) of group gi of the raw stage -> operand stage op.
-  __device__ static void convert(const uint8_t* raw, int, int r, int kq, uint8_t* op, float&) {
+  // TMEM lane r = weight row r of the tile.
+  __device__ static int raw_row(int r) { return r; }
+  // Row r of the stage's group -> 64 TMEM columns from tcol: chunk c (K 16c..16c+15)
+  // is MMA step c, natural pairs (16c + 2i, 16c + 2i + 1) in columns 8c + i.
+  template <int GI>
+  __device__ static void convert(const uint8_t* raw, int r, uint32_t tcol, float& d) {
     const uint8_t* row = raw + r * 128;
 #pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      const int c = kq * 2 + c2;                                   // 16-byte chunk = 16 K
-      const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
-      uint4 lo, hi;
-      e4m3x4_to_bf16(v.x, lo.x, lo.y);
-      e4m3x4_to_bf16(v.y, lo.z, lo.w);
-      e4m3x4_to_bf16(v.z, hi.x, hi.y);
-      e4m3x4_to_bf16(v.w, hi.z, hi.w);
-      *reinterpret_cast<uint4*>(op_chunk(op, r, 2 * c)) = lo;
-      *reinterpret_cast<uint4*>(op_chunk(op, r, 2 * c + 1)) = hi;
+    for (int h = 0; h < 4; ++h) {
+      uint32_t v[16];
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int c = 2 * h + c2;
+        const uint4 x = lds128(row + ((c ^ (r & 7)) << 4));
+        e4m3x4_to_bf16(x.x, v[8 * c2 + 0], v[8 * c2 + 1]);
+        e4m3x4_to_bf16(x.y, v[8 * c2 + 2], v[8 * c2 + 3]);
+        e4m3x4_to_bf16(x.z, v[8 * c2 + 4], v[8 * c2 + 5]);
+        e4m3x4_to_bf16(x.w, v[8 * c2 + 6], v[8 * c2 + 7]);
+      }
+      tmem_st16(tcol + 16 * h, v);
     }
+    d = 1.0f;
   }
 };
 
-// Q2_0: eight groups per raw stage, [128 rows x 8 blocks x 34 B], no swizzle.
+// Q2_0: eight groups per raw stage, [124 rows x 8 blocks x 34 B], no swizzle.
+// A row is 272 B = 68 words (68 = 4 mod 32), so 16-byte loads of 31
+// consecutive rows at the same offset are free of bank conflicts.
 struct Q2Tc {
+  static constexpr int kRows = 124;              // + an all-ones row per lane quarter
   static constexpr int kGPR = 8;
-  static constexpr int kSR = 2;
-  static constexpr int kSO = 3;
-  static constexpr int kRawBytes = BM * 8 * 34;
-  static constexpr bool kRowScale = true;
+  static constexpr int kSR = 3;
+  static constexpr int kRawBytes = BM * 8 * 34;  // stage stride
+  // TMEM lane r = 32 q + l holds weight row 31 q + l for l < 31; lane 31 of
+  // each quarter is the all-ones row.
+  __device__ static int raw_row(int r) { return (r >> 5) * 31 + (r & 31); }
+  static constexpr int kBoxBytes = kRows * 8 * 34;
+  static constexpr bool kQ2 = true;
+  static constexpr int kRawEmptyCount = 8;       // both converter sets
   __device__ static void issue_raw(const CUtensorMap* m, uint32_t dst, int g0, int n0, uint32_t bar,
                                    uint64_t pol) {
     tma_load_2d_hint(dst, m, g0 * 17, n0, bar, pol);              // 17 u16 per block
   }
-  __device__ static void convert(const uint8_t* raw, int gi, int r, int kq, uint8_t* op, float& d) {
-    const uint16_t* blk = reinterpret_cast<const uint16_t*>(raw + r * 272 + gi * 34);
-    if (kq == 0) d = __half2float(__ushort_as_half(blk[16]));
+  // Block GI of row r: its 34 bytes start OFF = 34 GI mod 16 bytes into a
+  // 48-byte window of three aligned 16-byte chunks. Word i of the block
+  // (codes 16i..16i+15) is MMA step i: columns 8i + j (j < 4) hold the pair
+  // (c_j, c_{j+8}) of the word, columns 8i + 4 + j the pair (c_{j+4}, c_{j+12}),
+  // both scaled by 4^j. The last lane of each quarter writes codes 1
+  // everywhere (it reads the quarter's first row and discards it).
+  template <int GI>
+  __device__ static void convert(const uint8_t* raw, int r, uint32_t tcol, float& d) {
+    constexpr int b0 = 34 * GI;
+    constexpr int base = b0 & ~15;
+    constexpr int off = b0 - base;                 // 0, 2, ..., 14
+    const bool ones = (r & 31) == 31;
+    const uint8_t* row = raw + raw_row(ones ? (r & ~31) : r) * 272 + base;
+    const uint4 c0 = lds128(row), c1 = lds128(row + 16), c2 = lds128(row + 32);
+    const uint32_t wv[12] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w, c2.x, c2.y, c2.z, c2.w};
 #pragma unroll
-    for (int w2 = 0; w2 < 2; ++w2) {
-      const int w = kq * 2 + w2;                                   // 16-code word of the block
-      const uint32_t q = static_cast<uint32_t>(blk[2 * w]) | (static_cast<uint32_t>(blk[2 * w + 1]) << 16);
-      uint32_t p[8];
-      q2_decode_word(q, p);                                        // p[j] = (c_j - 1, c_{j+8} - 1)
-      uint4 lo, hi;                                                // natural pairs (c_2i, c_2i+1)
-      lo.x = __byte_perm(p[0], p[1], 0x5410);
-      lo.y = __byte_perm(p[2], p[3], 0x5410);
-      lo.z = __byte_perm(p[4], p[5], 0x5410);
-      lo.w = __byte_perm(p[6], p[7], 0x5410);
-      hi.x = __byte_perm(p[0], p[1], 0x7632);
-      hi.y = __byte_perm(p[2], p[3], 0x7632);
-      hi.z = __byte_perm(p[4], p[5], 0x7632);
-      hi.w = __byte_perm(p[6], p[7], 0x7632);
-      *reinterpret_cast<uint4*>(op_chunk(op, r, 2 * w)) = lo;      // k = 16 w .. 16 w + 7
-      *reinterpret_cast<uint4*>(op_chunk(op, r, 2 * w + 1)) = hi;  // k = 16 w + 8 .. + 15
+    for (int h = 0; h < 4; ++h) {
+      uint32_t v[16];
+#pragma unroll
+      for (int w2 = 0; w2 < 2; ++w2) {
+        const int idx = off / 4 + 2 * h + w2;
+        uint32_t q = (off % 4 == 0) ? wv[idx] : __funnelshift_r(wv[idx], wv[idx + 1], 16);
+        q = ones ? 0x55555555u : q;
+        const uint32_t q8 = q >> 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * w2 + j] = q & (0x00030003u << (2 * j));
+          v[8 * w2 + 4 + j] = q8 & (0x00030003u << (2 * j));
+        }
+      }
+      tmem_st16(tcol + 16 * h, v);
     }
+    constexpr int dw = (off + 32) / 4;
+    const uint32_t dbits = (off % 4 == 0) ? (wv[dw] & 0xFFFFu) : (wv[dw] >> 16);
+    d = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
   }
 };
 
 template <class F>
 struct Layout {
-  static constexpr int kOpOff = 0;
-  static constexpr int kRawOff = kOpOff + F::kSO * kOpBytes;
-  static constexpr int kActOff = (kRawOff + F::kSR * F::kRawBytes + 1023) / 1024 * 1024;
-  static constexpr int kSclOff = kActOff + SA * kActBytes;
-  static constexpr int kBytes = kSclOff + NSCL * BM * 4;
-  static_assert(NSCL > F::kSO + NACC, "row-scale ring must outlive the pipeline");
+  static constexpr int kRawOff = 0;
+  static constexpr int kBOff = (kRawOff + F::kSR * F::kRawBytes + 1023) / 1024 * 1024;
+  static constexpr int kSclOff = kBOff + SB * kBBytes;
+  static constexpr int kBytes = kSclOff + (F::kQ2 ? NSC * BM * 4 : 0);
   static constexpr int kAlloc = kBytes + 1024;                     // slack for 1024-byte alignment
   static_assert(BM * BN * 4 <= F::kSR * F::kRawBytes, "split-K partials alias the raw ring");
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
+// All mbarriers of a CTA live in one shared array; Bar<F>::X is the index of
+// the first barrier of ring X, and bar(base, i) its shared-memory address.
 template <class F>
+struct Bar {
+  static constexpr int kRawFull = 0;                  // [SR]  raw stage landed
+  static constexpr int kRawEmpty = kRawFull + F::kSR; // [SR]  raw stage converted
+  static constexpr int kBLoad = kRawEmpty + F::kSR;   // [SB]  activation tile landed (Q2_0)
+  static constexpr int kGo = kBLoad + SB;             // [ND]  group j may start (kGoCount)
+  static constexpr int kDone = kGo + ND;              // [ND]  MMA of group j complete
+  static constexpr int kSclFull = kDone + ND;         // [NSC] row scales written
+  static constexpr int kCount = kSclFull + NSC;
+};
+__device__ __forceinline__ uint32_t bar(uint32_t base, int i) { return base + 8u * static_cast<uint32_t>(i); }
+
+// Convert group GI of raw stage t for this thread's row. False on abort.
+template <class F, int GI>
+__device__ __forceinline__ bool convert_group(const uint8_t* raw, int t, int q, int r, int lane,
+                                              uint32_t tmem, uint32_t bars, float* scl, unsigned* err,
+                                              volatile int* abort_flag) {
+  using B = Bar<F>;
+  const int j = t * F::kGPR + GI;
+  const int so = j % SO;
+  if (j >= SO) {
+    const int g = j - SO;                            // previous user of the stage
+    const bool ok = wait_or_abort(bar(bars, B::kDone + g % ND), (g / ND) & 1, err, abort_flag);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+  }
+  tc_fence_after();
+  float d;
+  F::template convert<GI>(raw, r, tmem + (static_cast<uint32_t>(q * 32) << 16) + so * 64, d);
+  tmem_wait_st();
+  if (F::kQ2) scl[(j % NSC) * BM + r] = d;
+  tc_fence_before();
+  __threadfence_block();
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(bar(bars, B::kGo + j % ND));
+    if (F::kQ2) mbar_arrive(bar(bars, B::kSclFull + j % NSC));
+  }
+  return true;
+}
+
+template <class F, int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
               TcParams p) {
   using L = Layout<F>;
   constexpr int SR = F::kSR;
-  constexpr int SO = F::kSO;
   constexpr int GPR = F::kGPR;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t raw_full[SR], raw_empty[SR];
-  __shared__ __align__(8) uint64_t act_full[SA], act_empty[SA];
-  __shared__ __align__(8) uint64_t op_full[SO], op_empty[SO];
-  __shared__ __align__(8) uint64_t acc_full[NACC], acc_empty[NACC];
-  __shared__ __align__(8) uint64_t scl_full[NSCL];
+  using B = Bar<F>;
+  __shared__ __align__(8) uint64_t bar_sh[B::kCount];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -171,201 +287,249 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int splits = p.splits;
   const int tile = blockIdx.x / splits;
   const int rank = blockIdx.x - tile * splits;      // == %cluster_ctarank
-  const int n0 = tile * BM;
+  const int n0 = tile * F::kRows;
   const int st_begin = (rank * p.stages) / splits;
   const int st_end = ((rank + 1) * p.stages) / splits;
   const int g_begin = st_begin * GPR;
-  const int ng = (st_end - st_begin) * GPR;          // groups of this CTA
   const int nst = st_end - st_begin;                 // raw stages of this CTA
+  const int ng = nst * GPR;                          // groups of this CTA
   volatile int* abort_flag = &abort_sh;
+  const uint32_t bars = smem_u32(bar_sh);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < SR; ++i) { mbar_init(smem_u32(&raw_full[i]), 1); mbar_init(smem_u32(&raw_empty[i]), kConvWarps); }
-    for (int i = 0; i < SA; ++i) { mbar_init(smem_u32(&act_full[i]), 1); mbar_init(smem_u32(&act_empty[i]), 1); }
-    for (int i = 0; i < SO; ++i) { mbar_init(smem_u32(&op_full[i]), kConvWarps); mbar_init(smem_u32(&op_empty[i]), 1); }
-    for (int i = 0; i < NACC; ++i) { mbar_init(smem_u32(&acc_full[i]), 1); mbar_init(smem_u32(&acc_empty[i]), 4); }
-    for (int i = 0; i < NSCL; ++i) mbar_init(smem_u32(&scl_full[i]), 4);
+    for (int i = 0; i < B::kCount; ++i) {
+      uint32_t count = 1;
+      if (i >= B::kRawEmpty && i < B::kBLoad) count = F::kRawEmptyCount;
+      if (i >= B::kGo && i < B::kDone) count = kGoCount;
+      if (i >= B::kSclFull) count = 4;
+      mbar_init(bar(bars, i), count);
+    }
+    // The accumulator slots start free: the epilogue's four releases for
+    // groups 0 .. NACC-1.
+    for (int i = 0; i < NACC; ++i)
+      for (int k = 0; k < 4; ++k) mbar_arrive(bar(bars, B::kGo + i));
     abort_sh = 0;
     mbar_fence_init();
   }
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
-    tmem_relinquish();
-  }
-  if (warp == kTmaWarp && lane == 0) {
-    prefetch_tmap(&tmW);
-    prefetch_tmap(&tmA);
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
   pdl_launch_dependents();
-  const uint32_t tmem = tmem_base_sh;
-
-  float acc[BN];
-#pragma unroll
-  for (int m = 0; m < BN; ++m) acc[m] = 0.0f;
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA
-    // Lane 0 streams raw weight stages, lane 1 streams activation tiles, so
-    // neither ring waits on the other.
+    // Lane 0 streams raw weight stages (independent of the previous grid, so
+    // they start before griddepcontrol.wait); lane 1 streams activation tiles.
     if (lane == 0) {
+      prefetch_tmap(&tmW);
       const uint64_t pol = policy_evict_first();
       int raw_issued = 0;
       for (int t = 0; t < nst; ++t) {
         const int sr = t % SR;
-        if (t >= SR && !wait_or_abort(smem_u32(&raw_empty[sr]), ((t / SR) - 1) & 1, p.err, abort_flag)) break;
-        mbar_arrive_expect_tx(smem_u32(&raw_full[sr]), F::kRawBytes);
+        if (t >= SR && !wait_or_abort(bar(bars, B::kRawEmpty + sr), ((t / SR) - 1) & 1, p.err, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(bars, B::kRawFull + sr), F::kBoxBytes);
         F::issue_raw(&tmW, sbase + L::kRawOff + sr * F::kRawBytes, g_begin + t * GPR, n0,
-                     smem_u32(&raw_full[sr]), pol);
+                     bar(bars, B::kRawFull + sr), pol);
         raw_issued = t + 1;
       }
       // Drain: every issued copy has landed before the CTA may exit.
       for (int t = max(0, raw_issued - SR); t < raw_issued; ++t)
-        mbar_wait(smem_u32(&raw_full[t % SR]), (t / SR) & 1, p.err);
+        mbar_wait(bar(bars, B::kRawFull + t % SR), (t / SR) & 1, p.err);
     } else if (lane == 1) {
-      pdl_wait();                          // activations may come from the previous kernel
-      int act_issued = 0;
-      for (int j = 0; j < ng; ++j) {
-        const int sa = j % SA;
-        if (j >= SA && !wait_or_abort(smem_u32(&act_empty[sa]), ((j / SA) - 1) & 1, p.err, abort_flag)) break;
-        mbar_arrive_expect_tx(smem_u32(&act_full[sa]), kActBytes);
-        const uint32_t dst = sbase + L::kActOff + sa * kActBytes;
-        tma_load_2d(dst, &tmA, (g_begin + j) * GK, 0, smem_u32(&act_full[sa]));
-        tma_load_2d(dst + kActBytes / 2, &tmA, (g_begin + j) * GK + 64, 0, smem_u32(&act_full[sa]));
-        act_issued = j + 1;
-      }
-      for (int j = max(0, act_issued - SA); j < act_issued; ++j)
-        mbar_wait(smem_u32(&act_full[j % SA]), (j / SA) & 1, p.err);
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      // Activation tiles [16 rows x 128 K] (rows >= M zero-filled) into the
+      // operand ring; Q2_0 tiles are rewritten in place by the preparation
+      // warps before the MMA reads them.
+      prefetch_tmap(&tmA);
+      pdl_wait();                          // activations may come from the previous grid
       int issued = 0;
       for (int j = 0; j < ng; ++j) {
-        const int so = j % SO, sa = j % SA, sc = j % NACC;
-        if (!wait_or_abort(smem_u32(&op_full[so]), (j / SO) & 1, p.err, abort_flag)) break;
-        if (!wait_or_abort(smem_u32(&act_full[sa]), (j / SA) & 1, p.err, abort_flag)) break;
-        if (j >= NACC && !wait_or_abort(smem_u32(&acc_empty[sc]), ((j / NACC) - 1) & 1, p.err, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t opb = sbase + L::kOpOff + so * kOpBytes;
-        const uint32_t actb = sbase + L::kActOff + sa * kActBytes;
-#pragma unroll
-        for (int i = 0; i < GK / 16; ++i) {
-          // Weights: 128-byte swizzled K-major blocks of 64 K (see op_chunk);
-          // 32 B per 16-K step; SBO = 1024 B (8-row atoms).
-          const uint64_t ad = sdesc(opb + (i >> 2) * (BM * 128) + (i & 3) * 32, 16, 1024, 2);
-          // Activations: 128-byte swizzled rows of 64 K; 32 B per 16-K step,
-          // the second 64 K in the second box; SBO = 1024 B (8-row atoms).
-          const uint64_t bd = sdesc(actb + (i >> 2) * (kActBytes / 2) + (i & 3) * 32, 16, 1024, 2);
-          mma_bf16(tmem + sc * 16, ad, bd, idesc, i > 0 ? 1u : 0u);
+        const int s = j % SB;
+        const int full = B::kBLoad + s;
+        if (j >= SB) {
+          const int g = j - SB;            // previous user of the stage
+          if (!wait_or_abort(bar(bars, B::kDone + g % ND), (g / ND) & 1, p.err, abort_flag)) break;
         }
-        mma_commit(smem_u32(&op_empty[so]));
-        mma_commit(smem_u32(&act_empty[sa]));
-        mma_commit(smem_u32(&acc_full[sc]));
+        mbar_arrive_expect_tx(bar(bars, full), kBBytes);
+        const uint32_t dst = sbase + L::kBOff + s * kBBytes;
+        tma_load_2d(dst, &tmA, (g_begin + j) * GK, 0, bar(bars, full));
+        tma_load_2d(dst + kBBytes / 2, &tmA, (g_begin + j) * GK + 64, 0, bar(bars, full));
         issued = j + 1;
       }
-      // Drain: all MMAs done before TMEM is freed.
-      if (issued > 0) {
-        const int j = issued - 1;
-        mbar_wait(smem_u32(&acc_full[j % NACC]), (j / NACC) & 1, p.err);
-      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      for (int j = max(0, issued - SB); j < issued; ++j)
+        mbar_wait(bar(bars, B::kBLoad + j % SB), (j / SB) & 1, p.err);
     }
-  } else if (warp < kConvWarps) {
-    // ------------------------------------------------------------ convert
-    const int q = warp & 3;                 // row block
-    const int kq = warp >> 2;               // which 32-K quarter of a group
-    const int r = q * 32 + lane;            // row within the tile
-    float* scl = reinterpret_cast<float*>(smem + L::kSclOff);     // [NSCL][BM] row scales
+  } else {
+    // Everyone else needs the TMEM base address.
+    if (warp == kMmaWarp) {
+      tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+      tmem_relinquish();
+      tc_fence_before();
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
+    tc_fence_after();
+  }
+  const uint32_t tmem = (warp == kTmaWarp) ? 0u : tmem_base_sh;
+  // Partial sums [NB][BM] for the final reduction alias the raw ring: the
+  // epilogue writes them after the MMA of the last group completed, so every
+  // raw stage has been consumed by then.
+  float* red = reinterpret_cast<float*>(smem + L::kRawOff);
+
+  if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA
+    constexpr uint32_t idesc = idesc_bf16(BM, BN);
+    const uint32_t b_base = sbase + L::kBOff;
+    int issued = 0;
     for (int j = 0; j < ng; ++j) {
-      const int t = j / GPR, gi = j % GPR;
-      const int sr = t % SR, so = j % SO;
-      const bool g1 = (gi != 0) || wait_or_abort(smem_u32(&raw_full[sr]), (t / SR) & 1, p.err, abort_flag);
-      const bool g2 = g1 && (j < SO || wait_or_abort(smem_u32(&op_empty[so]), ((j / SO) - 1) & 1, p.err, abort_flag));
-      if (!__all_sync(0xFFFFFFFFu, g1 && g2)) break;
-      float d = 0.0f;
-      F::convert(smem + L::kRawOff + sr * F::kRawBytes, gi, r, kq, smem + L::kOpOff + so * kOpBytes, d);
-      // Slot j % NSCL is free: its previous group was folded before this
-      // group's operand stage could be released (pipeline depth SO + NACC).
-      if (F::kRowScale && kq == 0) scl[(j % NSCL) * BM + r] = d;
-      fence_proxy_async_smem();
-      __threadfence_block();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&op_full[so]));
-        if (gi == GPR - 1) mbar_arrive(smem_u32(&raw_empty[sr]));
-        if (F::kRowScale && kq == 0) mbar_arrive(smem_u32(&scl_full[j % NSCL]));
+      const bool ok = wait_or_abort(bar(bars, B::kGo + j % ND), (j / ND) & 1, p.err, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      if (elect_one()) {
+        // B: two 128-byte-swizzled boxes of 64 K (2 KB apart), 32 B per
+        // 16-K step, SBO = 1024 B (8-row atoms). The start-address field is
+        // address >> 4, so a step adds 2 and a box adds 128 (no carry:
+        // shared addresses stay below 2^18).
+        const uint64_t bd0 = sdesc(b_base + (j % SB) * kBBytes, 16, 1024, 2);
+        const uint32_t a0 = tmem + (j % SO) * 64;
+        const uint32_t dcol = tmem + kAccCol + (j % NACC) * 16;
+#pragma unroll
+        for (int i = 0; i < GK / 16; ++i)
+          mma_ts(dcol, a0 + 8 * i, bd0 + static_cast<uint64_t>((i >> 2) * 128 + (i & 3) * 2), idesc,
+                 i > 0 ? 1u : 0u);
+        mma_commit(bar(bars, B::kDone + j % ND));
       }
+      __syncwarp();
+      issued = j + 1;
+    }
+    // Drain: all MMAs done before TMEM is freed.
+    if (issued > 0) {
+      const int j = issued - 1;
+      mbar_wait(bar(bars, B::kDone + j % ND), (j / ND) & 1, p.err);
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ convert
+    const int q = warp & 3;                 // TMEM lane quarter = 32-row block
+    const int h = warp >> 2;                // group parity
+    const int r = q * 32 + lane;
+    float* scl = reinterpret_cast<float*>(smem + L::kSclOff);
+    for (int t = (GPR == 1 ? h : 0); t < nst; t += (GPR == 1 ? 2 : 1)) {
+      const int sr = t % SR;
+      const bool got = wait_or_abort(bar(bars, B::kRawFull + sr), (t / SR) & 1, p.err, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, got)) break;
+      const uint8_t* raw = smem + L::kRawOff + sr * F::kRawBytes;
+      bool live;
+#define WQP_CONV(GI) convert_group<F, GI>(raw, t, q, r, lane, tmem, bars, scl, p.err, abort_flag)
+      if constexpr (GPR == 1) {
+        live = WQP_CONV(0);
+      } else if (h == 0) {
+        live = WQP_CONV(0) && WQP_CONV(2) && WQP_CONV(4) && WQP_CONV(6);
+      } else {
+        live = WQP_CONV(1) && WQP_CONV(3) && WQP_CONV(5) && WQP_CONV(7);
+      }
+#undef WQP_CONV
+      if (!live) break;
+      if (lane == 0) mbar_arrive(bar(bars, B::kRawEmpty + sr));
     }
   } else if (warp < kEpiWarp0 + 4) {
     // ------------------------------------------------------------ fold
-    const int q = warp & 3;                 // TMEM lane quarter
+    const int q = warp & 3;
     const int r = q * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol;
     const float* scl = reinterpret_cast<const float*>(smem + L::kSclOff);
-    const float* srow = F::kRowScale ? nullptr : p.scales + static_cast<size_t>(tile) * (p.K / GK);
+    const float* srow = F::kQ2 ? nullptr : p.scales + static_cast<size_t>(tile) * (p.K / GK);
+    float acc[NB];
+#pragma unroll
+    for (int m = 0; m < NB; ++m) acc[m] = 0.0f;
     for (int j = 0; j < ng; ++j) {
-      const int sc = j % NACC;
+      const int sc = j % NACC, nsc = j % NSC;
+      bool got = wait_or_abort(bar(bars, B::kDone + j % ND), (j / ND) & 1, p.err, abort_flag);
+      if (F::kQ2) got = got && wait_or_abort(bar(bars, B::kSclFull + nsc), (j / NSC) & 1, p.err, abort_flag);
       // Warp-uniform outcome: tcgen05.ld below is .sync.aligned.
-      const bool got = wait_or_abort(smem_u32(&acc_full[sc]), (j / NACC) & 1, p.err, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
-      float v[16];
-      tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + sc * 16, v);
+      float v[NB];
+      tmem_ld<NB>(tl + sc * 16, v);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[sc]));
-      float s;
-      if (F::kRowScale) {
-        const bool gs = wait_or_abort(smem_u32(&scl_full[j % NSCL]), (j / NSCL) & 1, p.err, abort_flag);
-        if (!__all_sync(0xFFFFFFFFu, gs)) break;
-        s = scl[(j % NSCL) * BM + r];
-      } else {
-        s = __ldg(srow + g_begin + j);
-      }
+      if (lane == 0) mbar_arrive(bar(bars, B::kGo + (j + NACC) % ND));   // slot free for j + NACC
+      if (F::kQ2) {
+        // Lane 31 of the warp (the all-ones row) holds 2^-69 * sum_k a[m, k].
+        const float d69 = scl[nsc * BM + r] * 0x1p69f;
 #pragma unroll
-      for (int m = 0; m < BN; ++m) acc[m] = fmaf(v[m], s, acc[m]);
+        for (int m = 0; m < NB; ++m) acc[m] = fmaf(d69, v[m] - __shfl_sync(0xFFFFFFFFu, v[m], 31), acc[m]);
+      } else {
+        const float s = __ldg(srow + g_begin + j);
+#pragma unroll
+        for (int m = 0; m < NB; ++m) acc[m] = fmaf(v[m], s, acc[m]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < NB; ++m) red[m * BM + r] = acc[m];
+  } else if (warp >= kPrepWarp0) {
+    // ------------------------------------------------------------ operand hand-off
+    // Warp p prepares groups j = p mod 2. Thread (row m, half) rewrites MMA
+    // steps 4 half .. 4 half + 3 in place: the natural chunks
+    // k = 16i..16i+7 and 16i+8..16i+15 of row m become the pairs
+    // (16i + c', 16i + c' + 8), c' = 0..7, times 2^(64 - 2 (c' mod 4)).
+    const int pw = warp - kPrepWarp0;
+    const int m = lane >> 1;
+    const int half = lane & 1;
+    const bool act = m < p.M;
+    constexpr uint32_t kS0 = 0x5F805F80u, kS1 = 0x5E805E80u, kS2 = 0x5D805D80u, kS3 = 0x5C805C80u;
+    for (int j = pw; j < ng; j += kPrepWarps) {
+      const int sb = j % SB;
+      const bool got = wait_or_abort(bar(bars, B::kBLoad + sb), (j / SB) & 1, p.err, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, got)) break;
+      if (F::kQ2 && act) {
+        uint8_t* rowp = smem + L::kBOff + sb * kBBytes + half * (kBBytes / 2) + m * 128;
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          uint8_t* p0 = rowp + (((2 * st) ^ (m & 7)) << 4);
+          uint8_t* p1 = rowp + (((2 * st + 1) ^ (m & 7)) << 4);
+          const uint4 x = lds128(p0);
+          const uint4 y = lds128(p1);
+          uint4 o0, o1;
+          o0.x = mul_bf16x2(__byte_perm(x.x, y.x, 0x5410), kS0);
+          o0.y = mul_bf16x2(__byte_perm(x.x, y.x, 0x7632), kS1);
+          o0.z = mul_bf16x2(__byte_perm(x.y, y.y, 0x5410), kS2);
+          o0.w = mul_bf16x2(__byte_perm(x.y, y.y, 0x7632), kS3);
+          o1.x = mul_bf16x2(__byte_perm(x.z, y.z, 0x5410), kS0);
+          o1.y = mul_bf16x2(__byte_perm(x.z, y.z, 0x7632), kS1);
+          o1.z = mul_bf16x2(__byte_perm(x.w, y.w, 0x5410), kS2);
+          o1.w = mul_bf16x2(__byte_perm(x.w, y.w, 0x7632), kS3);
+          *reinterpret_cast<uint4*>(p0) = o0;
+          *reinterpret_cast<uint4*>(p1) = o1;
+        }
+      }
+      fence_proxy_async_smem();
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(bars, B::kGo + j % ND));
     }
   }
 
   // ---------------------------------------------------------- reduce + store
   __syncthreads();
   const bool failed = *abort_flag != 0;
-  float* red = reinterpret_cast<float*>(smem + L::kRawOff);   // raw ring is idle now
-  if (splits > 1) {
-    const bool epi = warp >= kEpiWarp0 && warp < kEpiWarp0 + 4;
-    const int er = (warp - kEpiWarp0) * 32 + lane;
-    if (epi && rank != 0) {
-      float4* dst = reinterpret_cast<float4*>(red + er * BN);
+  const bool epi = warp >= kEpiWarp0 && warp < kEpiWarp0 + 4;
+  const int er = (warp - kEpiWarp0) * 32 + lane;
+  if (splits > 1) cluster_sync();         // every rank's partials are in its shared memory
+  if (epi && rank == 0 && !failed && F::raw_row(er) < F::kRows && !(F::kQ2 && (er & 31) == 31)) {
+    const int n = n0 + F::raw_row(er);
+    const uint32_t mine = smem_u32(red + er);
 #pragma unroll
-      for (int i = 0; i < BN / 4; ++i) dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-    }
-    cluster_sync();
-    if (epi && rank == 0) {
-      const uint32_t mine = smem_u32(red + er * BN);
-      for (int qq = 1; qq < splits; ++qq) {
-        const uint32_t rem = mapa_shared(mine, qq);
-#pragma unroll
-        for (int i = 0; i < BN / 4; ++i) {
-          const float4 v = ld_dsmem_f4(rem + 16 * i);
-          acc[4 * i] += v.x;
-          acc[4 * i + 1] += v.y;
-          acc[4 * i + 2] += v.z;
-          acc[4 * i + 3] += v.w;
-        }
+    for (int m = 0; m < NB; ++m) {
+      float acc = red[m * BM + er];
+      for (int qq = 1; qq < splits; ++qq) {      // rank order: deterministic
+        float v;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                     : "=f"(v)
+                     : "r"(mapa_shared(mine, qq) + m * BM * 4)
+                     : "memory");
+        acc += v;
       }
-    }
-    cluster_sync();                       // remote partials stay alive until read
-  }
-  if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4 && rank == 0 && !failed) {
-    const int n = n0 + (warp - kEpiWarp0) * 32 + lane;
-    if (n < p.N) {
-#pragma unroll
-      for (int m = 0; m < BN; ++m)
-        if (m < p.M) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc[m]);
+      if (m < p.M && n < p.N) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc);
     }
   }
+  if (splits > 1) cluster_sync();         // remote partials stay alive until read
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
@@ -374,40 +538,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
+// CTAs per tile: one wave of one CTA per SM (a kernel that allocates tensor
+// memory runs one CTA per SM), at most 8 (portable cluster size) and at most
+// one raw stage per CTA.
 int choose_splits(int tiles, int stages, int num_sms) {
-  int s = num_sms / tiles;                   // one CTA per SM, a single wave
+  int s = num_sms / tiles;
   if (s < 1) s = 1;
-  if (s > 8) s = 8;                          // portable cluster size
+  if (s > 8) s = 8;
   if (s > stages) s = stages;
   return s;
 }
 
-template <class F>
-cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, cudaStream_t s) {
+template <class F, int NB>
+cudaError_t launch_tc_nb(const CUtensorMap& mw, const CUtensorMap& ma, const TcParams& p, int tiles, bool pdl,
+                         cudaStream_t s) {
   using L = Layout<F>;
-  CUtensorMap ma;
-  cudaError_t e = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, static_cast<uint64_t>(a.K),
-                              static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda) * 2, 64, BN,
-                              CU_TENSOR_MAP_SWIZZLE_128B);
-  if (e != cudaSuccess) return e;
   static bool attr_set = false;
   if (!attr_set) {
-    e = cudaFuncSetAttribute(tc_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    cudaError_t e = cudaFuncSetAttribute(tc_kernel<F, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    // Two CTAs per SM need the whole shared-memory carveout.
+    e = cudaFuncSetAttribute(tc_kernel<F, NB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int tiles = (a.N + BM - 1) / BM;
-  TcParams p;
-  p.scales = static_cast<const float*>(a.scales);
-  p.C = static_cast<uint16_t*>(a.C);
-  p.M = a.M;
-  p.N = a.N;
-  p.K = a.K;
-  p.ldc = a.ldc;
-  p.stages = a.K / (GK * F::kGPR);
-  p.splits = choose_splits(tiles, p.stages, a.num_sms);
-  p.err = a.err;
-
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * p.splits);
   cfg.blockDim = dim3(kThreads);
@@ -420,14 +575,39 @@ cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, cudaStream_t s) 
   attr[na].val.clusterDim.y = 1;
   attr[na].val.clusterDim.z = 1;
   ++na;
-  if (a.pdl) {
+  if (pdl) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, tc_kernel<F>, mw, ma, p);
+  return cudaLaunchKernelEx(&cfg, tc_kernel<F, NB>, mw, ma, p);
+}
+
+template <class F>
+cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, cudaStream_t s) {
+  CUtensorMap ma;
+  cudaError_t e = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, static_cast<uint64_t>(a.K),
+                              static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda) * 2, 64, BN,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.N + F::kRows - 1) / F::kRows;
+  TcParams p;
+  p.scales = static_cast<const float*>(a.scales);
+  p.C = static_cast<uint16_t*>(a.C);
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.ldc = a.ldc;
+  p.stages = a.K / (GK * F::kGPR);
+  p.splits = choose_splits(tiles, p.stages, a.num_sms);
+  p.err = a.err;
+  if (a.M <= 1) return launch_tc_nb<F, 1>(mw, ma, p, tiles, a.pdl, s);
+  if (a.M <= 2) return launch_tc_nb<F, 2>(mw, ma, p, tiles, a.pdl, s);
+  if (a.M <= 4) return launch_tc_nb<F, 4>(mw, ma, p, tiles, a.pdl, s);
+  if (a.M <= 8) return launch_tc_nb<F, 8>(mw, ma, p, tiles, a.pdl, s);
+  return launch_tc_nb<F, 16>(mw, ma, p, tiles, a.pdl, s);
 }
 
 }  // namespace tc
@@ -450,7 +630,7 @@ cudaError_t launch_q2_gemm_tc(const GemvArgs& a, cudaStream_t s) {
   const uint64_t G = static_cast<uint64_t>(a.K / GK);
   CUtensorMap mw;
   cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),
-                              34 * G, 8 * 17, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                              34 * G, 8 * 17, Q2Tc::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   return launch_tc<Q2Tc>(a, mw, s);
 }
