@@ -36,8 +36,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "effective weight-stream GB/s (% of GB300 HBM peak) and us/call at M=1..16"
 UNIT = "GB/s"
-HEADLINE = {"fmt": "q2", "N": 5120, "K": 5120, "Ms": (1, 4, 8)}
-KERNEL_SOURCES = ["gemv_scalar.cuh", "gemv_q2.cu", "decode.cuh", "common.cuh"]
+# The step calls, for each M, the library's faster Q2_0 path at this shape
+# (measured): the scalar GEMV at M = 1, the tensor-core GEMM at M = 4 and 8.
+HEADLINE = {"fmt": "q2", "N": 5120, "K": 5120, "Ms": (1, 4, 8), "tc": {1: False, 4: True, 8: True}}
+KERNEL_SOURCES = {False: ["gemv_scalar.cuh", "gemv_q2.cu", "decode.cuh", "common.cuh"],
+                  True: ["gemm_tc.cu", "tc.cuh", "decode.cuh", "common.cuh"]}
 
 
 # ------------------------------------------------------------------ helpers
@@ -113,22 +116,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def source_hash():
+def source_hash(tc=False):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[tc]:
         with open(os.path.join(ROOT, "weight_only_quantized_packed_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel_key):
+def committed_traffic(kernel_key, tc=False):
     """dram bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources; else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         e = d.get(kernel_key)
-        if e and e.get("source_hash") == source_hash():
+        if e and e.get("source_hash") == source_hash(tc):
             return e["dram_bytes_per_launch"]
     except Exception:
         pass
@@ -184,20 +187,21 @@ class Workload:
         self.C = {M: torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for M in self.Ms}
         self.i = 0
 
-    def call(self, M, A=None, C=None):
+    def call(self, M, A=None, C=None, tc=None):
         import weight_only_quantized_packed_gb300 as wqp
 
         j = self.i % self.nbuf
         self.i += 1
         A = self.A[M] if A is None else A
         C = self.C[M] if C is None else C
-        if self.fmt == "q2" and self.tc:
+        tc = self.tc if tc is None else tc
+        if self.fmt == "q2" and tc:
             wqp.q2_gemm_tc(A, self.W[j], self.N, self.K, out=C)
         elif self.fmt == "q2":
             wqp.q2_gemv(A, self.W[j], self.N, self.K, out=C)
         elif self.fmt == "w4":
             wqp.w4a16_gemv(A, self.W[j], self.S[j], self.N, self.K, out=C)
-        elif self.tc:
+        elif tc:
             wqp.w8a16_gemm_tc(A, self.W[j], self.S[j], self.N, self.K, out=C)
         else:
             wqp.w8a16_gemm(A, self.W[j], self.S[j], self.N, self.K, out=C)
@@ -206,20 +210,48 @@ class Workload:
         self.W = self.S = self.A = self.C = None
 
 
-def time_calls(fn, n, warm=20):
+class GraphSteps:
+    """n calls of fn captured once into a CUDA graph (launch attributes such
+    as programmatic dependent launch are captured with them); replay() runs
+    them with no host work in between."""
+
+    def __init__(self, fn, n, warm=3):
+        import torch
+
+        self.n = n
+        self.stream = torch.cuda.Stream()
+        with torch.cuda.stream(self.stream):
+            for _ in range(warm):
+                fn()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            for _ in range(n):
+                fn()
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
+
+
+def time_calls(fn, n, warm=3, reps=3):
+    """Device time per call (us): a graph of n calls, median of reps replays."""
     import torch
 
-    for _ in range(warm):
-        fn()
+    g = GraphSteps(fn, n, warm)
+    g.replay()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(n):
-        fn()
-    e1.record()
-    e1.synchronize()
-    return e0.elapsed_time(e1) * 1e3 / n   # us per call
+    out = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e3 / n)
+    del g
+    return statistics.median(out)
 
 
 def sweep(l2, peak):
@@ -232,7 +264,7 @@ def sweep(l2, peak):
     specs = [
         ("q2_gemv N=256 K=512", "q2", 256, 512, (1,), False, 0),
         ("q2_gemv N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), False, 1),
-        ("q2_gemm_tc N=5120 K=5120", "q2", 5120, 5120, (1, 8, 16), True, 1),
+        ("q2_gemm_tc N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), True, 1),
         ("w4a16_gemv N=5120 K=5120", "w4", 5120, 5120, tuple(range(1, 9)), False, 2),
         ("w8a16_gemm N=17408 K=5120", "w8", 17408, 5120, (1, 4, 8, 16), False, 3),
         ("w8a16_gemm N=5120 K=17408", "w8", 5120, 17408, (1, 4, 8, 16), False, 3),
@@ -244,13 +276,14 @@ def sweep(l2, peak):
         for name, fmt, N, K, Ms, tc, wl in specs:
             w = Workload(fmt, N, K, Ms, l2, wl, tc=tc)
             for M in Ms:
-                us = time_calls(lambda: w.call(M), max(50, min(2000, int(2e5 / max(1, w.wb // 4096)))))
+                us = time_calls(lambda: w.call(M), max(20, min(400, int(2e5 / max(1, w.wb // 4096)))))
                 gbs = w.wb / us / 1e3
                 out.append({"workload": name, "M": M, "us": round(us, 3), "gbs": round(gbs, 1),
                             "pct_peak": round(100 * gbs / peak, 1)})
             w.free()
             torch.cuda.empty_cache()
-        # Decoder-layer sequence: qkv, o, gate+up, down, 8 layers cycled.
+        # Decoder-layer sequence: qkv, o, gate+up, down, 8 layers cycled;
+        # scalar at M = 1, tensor core above.
         layer = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
         ws = [Workload("q2", N, K, (1, 4, 8, 16), 0, 4, cap_bytes=0) for (N, K) in layer]
         for w in ws:
@@ -258,8 +291,9 @@ def sweep(l2, peak):
             w.W = [w.W[0]] + [w.W[0].clone() for _ in range(7)]
         lb = sum(w.wb for w in ws)
         for M in (1, 4, 8, 16):
-            us = time_calls(lambda: [w.call(M) for w in ws], 100)
+            us = time_calls(lambda: [w.call(M, tc=M > 1) for w in ws], 40)
             out.append({"workload": "q2 decoder layer (qkv+o+gate_up+down), 8 layers cycled", "M": M,
+                        "path": "q2_gemv" if M == 1 else "q2_gemm_tc",
                         "us_per_layer": round(us, 3), "gbs": round(lb / us / 1e3, 1),
                         "pct_peak": round(100 * lb / us / 1e3 / peak, 1)})
         del ws
@@ -293,70 +327,67 @@ def gpu_arm(args, rank, world, local_rank):
 
     def step():
         for M in H["Ms"]:
-            w.call(M)
+            w.call(M, tc=H["tc"][M])
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    # The timed steps run as replays of a CUDA graph of G steps (no host work
+    # between calls, as a decode loop would run them).
+    G = 100 if args.steps % 100 == 0 else (50 if args.steps % 50 == 0 else args.steps)
+    steps_graph = GraphSteps(step, G)
     if dist:
         dist.barrier()
-    stream = torch.cuda.current_stream()
     with ClockSampler(dev) as clk:
         # Keep the clock sampler's window filled with work before and after.
         t_end = time.time() + 0.3
         while time.time() < t_end:
-            step()
+            steps_graph.replay()
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
+        stream = steps_graph.stream
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps // G):
+                steps_graph.replay()
+            e1.record(stream)
         e1.synchronize()
         if dist:
             dist.barrier()
         ms_total = e0.elapsed_time(e1)
-        # Per-kernel durations of the same launches (events around each call).
-        per = {M: [] for M in H["Ms"]}
-        n_inst = min(args.steps, 2000)
-        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in H["Ms"]] for _ in range(n_inst)]
-        for s in range(n_inst):
-            for (a, b), M in zip(ev[s], H["Ms"]):
-                a.record(stream)
-                w.call(M)
-                b.record(stream)
-        torch.cuda.synchronize()
-        for s in range(n_inst):
-            for (a, b), M in zip(ev[s], H["Ms"]):
-                per[M].append(a.elapsed_time(b) * 1e3)
+        # Per-kernel durations: each call of the step alone, as a graph of
+        # back-to-back calls (events on the launching stream around it).
+        avg = {M: time_calls(lambda M=M: w.call(M, tc=H["tc"][M]), 200) for M in H["Ms"]}
+    del steps_graph
     wqp.set_pdl(False)
     ms_total = reduce_max_ms(ms_total, dist)
     ms_step = ms_total / args.steps
     value = job_value(bytes_step, args.steps, world, ms_total)
 
     # Dominant kernel: the call with the largest average duration.
-    avg = {M: statistics.fmean(v) for M, v in per.items()}
     Mdom = max(avg, key=avg.get)
     us_dom = avg[Mdom]
+    tc_dom = H["tc"][Mdom]
+    kname = "q2_gemm_tc" if tc_dom else "q2_gemv"
     achieved = w.wb / (us_dom * 1e-6) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                "kernel": f"q2_gemv M={Mdom} N={H['N']} K={H['K']}",
+                "kernel": f"{kname} M={Mdom} N={H['N']} K={H['K']}",
                 "algorithmic_bytes_per_launch": w.wb,
-                "traffic": committed_traffic(f"q2_gemv_M{Mdom}_N{H['N']}_K{H['K']}")}
+                "traffic": committed_traffic(f"{kname}_M{Mdom}_N{H['N']}_K{H['K']}", tc_dom)}
     # ALU view of the same kernel: useful FMAs per second over the FP32 FMA peak.
     sm_count = props.multi_processor_count
     clk_sum = clk.summary()
     f_mhz = clk_sum["sm_mhz"] or sm_max_nominal
     fma_peak = sm_count * 128 * f_mhz * 1e6 / 1e12
-    roofline["alu_view"] = {"fma_tflops_achieved": round(Mdom * H["N"] * H["K"] / (us_dom * 1e-6) / 1e12, 3),
-                            "fma_tflops_peak": round(fma_peak, 2), "unit": "T FMA/s",
-                            "frac": round(Mdom * H["N"] * H["K"] / (us_dom * 1e-6) / 1e12 / fma_peak, 4),
-                            "peak_from": f"{sm_count} SMs x 128 FP32 lanes x {f_mhz:.0f} MHz"}
+    if not tc_dom:
+        roofline["alu_view"] = {"fma_tflops_achieved": round(Mdom * H["N"] * H["K"] / (us_dom * 1e-6) / 1e12, 3),
+                                "fma_tflops_peak": round(fma_peak, 2), "unit": "T FMA/s",
+                                "frac": round(Mdom * H["N"] * H["K"] / (us_dom * 1e-6) / 1e12 / fma_peak, 4),
+                                "peak_from": f"{sm_count} SMs x 128 FP32 lanes x {f_mhz:.0f} MHz"}
 
     # End-to-end through the C ABI with host buffers (pinned): per step copy
     # the three activation blocks in, compute, copy the three outputs back.
@@ -368,7 +399,9 @@ def gpu_arm(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; A ~ N(0,1) bf16, ternary codes U{0,1,2}, d U[0.01,0.05] fp16)",
-        "config": {"workload": "q2_gemv N=5120 K=5120, one step = M=1, 4, 8 calls",
+        "config": {"workload": "Q2_0 GEMV N=5120 K=5120, one step = M=1, 4, 8 calls",
+                   "paths": {str(M): ("q2_gemm_tc" if H["tc"][M] else "q2_gemv") for M in H["Ms"]},
+                   "timing": f"CUDA graph of {G} steps replayed {args.steps // G} times",
                    "weight_bytes_per_call": w.wb, "weight_buffers_cycled": w.nbuf,
                    "l2": f"inputs larger than L2: {w.nbuf} weight buffers = {w.nbuf * w.wb / 2**20:.0f} MiB > 3x L2 ({l2 / 2**20:.0f} MiB)",
                    "pdl": bool(args.pdl), "parallelism": f"replicas x{world}"},
@@ -401,7 +434,7 @@ def e2e_arm(w, H, steps):
     def step():
         for M in H["Ms"]:
             dA[M].copy_(hA[M], non_blocking=True)
-            w.call(M, A=dA[M])
+            w.call(M, A=dA[M], tc=H["tc"][M])
             hC[M].copy_(w.C[M], non_blocking=True)
 
     for _ in range(5):
