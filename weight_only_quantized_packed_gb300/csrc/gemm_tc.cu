@@ -37,25 +37,27 @@
 //
 // One CTA = one tile of weight rows x a contiguous range of 128-K groups (a
 // multiple of the raw stage). Warps:
-//   0..7   converters, in two sets (group parity = warp / 4), TMEM lane
-//          quarter = warp % 4; each thread converts one weight row of one
-//          group (64 columns);
-//   8..11  epilogue: per group, tcgen05.ld of the group's accumulator slot
-//          (lane = weight row, column = activation row) and the FP32 fold;
-//   12     TMA: lane 0 raw weight stages, lane 1 activation tiles;
-//   13     MMA: allocates TMEM; per group one wait, then the elected lane
-//          issues the 8 MMAs into the group's accumulator slot and commits
-//          once ("MMA of group j done");
-//   14..15 activation operand hand-off (alternate groups): Q2_0 tiles are
+//   0..15  converters, in four sets (set = warp / 4 takes groups j = set
+//          mod 4), TMEM lane quarter = warp % 4; each thread converts one
+//          weight row of one group (64 columns);
+//   16..23 epilogue, two sets of four (alternate groups): per group,
+//          tcgen05.ld of the group's accumulator slot (lane = weight row,
+//          column = activation row) and the FP32 fold; each set keeps its own
+//          partial sums, added in a fixed order at the end;
+//   24     TMA: lane 0 raw weight stages, lane 1 activation tiles;
+//   25..26 MMA (alternate groups; 25 allocates TMEM): per group one wait,
+//          then the elected lane issues the 8 MMAs into the group's
+//          accumulator slot and commits once ("MMA of group j done");
+//   27..28 activation operand hand-off (alternate groups): Q2_0 tiles are
 //          prepared in place on the tile the TMA loaded; FP8 tiles are used
 //          as loaded.
 // The MMA warp waits on a single barrier per group, "group j may start",
 // which completes after nine arrivals: the four converter warps of the set,
 // the activation operand (its hand-off warp) and
 // the four epilogue warps releasing the accumulator slot (pre-armed for the
-// first NACC groups). A warp that issues MMAs stalls at its next
-// shared-memory access until the tensor core has taken them, so the MMA
-// warp does nothing else.
+// first NACC groups). Every mbarrier wait costs a warp about 150 cycles of
+// latency even when the phase has completed, so a role keeps several groups
+// in flight by spreading them over several warps.
 // Q2_0 tiles are 124 weight rows: the last lane of each 32-lane quarter of
 // TMEM (lanes 31, 63, 95, 127) holds a row of all-ones codes, whose
 // accumulator is 2^-69 * sum_k a_k, the group sum the fold needs, computed by
@@ -73,12 +75,16 @@ namespace tc {
 constexpr int BM = 128;            // TMEM lanes = MMA M
 constexpr int BN = 16;             // activation rows (MMA N)
 constexpr int GK = 128;            // K per group = scale granularity
-constexpr int kEpiWarp0 = 8;       // epilogue warps 8..11
-constexpr int kTmaWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kPrepWarp0 = 14;     // activation hand-off warps 14..15
+constexpr int kConvSets = 4;       // converter warps 0..15
+constexpr int kEpiWarp0 = 16;      // epilogue warps 16..23, two sets
+constexpr int kEpiSets = 2;
+constexpr int kTmaWarp = 24;
+constexpr int kMmaWarp = 25;       // MMA warps 25..26; 25 allocates TMEM
+constexpr int kMmaWarps = 2;
+constexpr int kMmaBatch = 1;       // groups issued per wait of the MMA warp
+constexpr int kPrepWarp0 = 27;     // activation hand-off warps 27..28
 constexpr int kPrepWarps = 2;
-constexpr int kThreads = 16 * 32;
+constexpr int kThreads = 29 * 32;
 constexpr int SO = 6;              // TMEM operand stages, one group (64 columns) each
 constexpr int NACC = 8;            // TMEM accumulator slots, 16 columns each
 constexpr uint32_t kAccCol = SO * 64;
@@ -97,6 +103,7 @@ constexpr int NSC = 16;            // per-group row-scale ring (converters -> ep
 // parities never alias.
 static_assert(NSC >= SO + NACC, "scale ring must outlive the pipeline");
 static_assert(ND >= SB && ND >= SO && ND > NACC, "done ring depth");
+static_assert(kMmaBatch <= NACC && kMmaBatch <= SO, "the MMA warp waits for a batch of groups at once");
 // "Group j may start" slot j % ND receives arrivals for group j only after the
 // MMA of group j - ND was issued: converters wait for MMA j - SO, the operand
 // producer for MMA j - SB, the epilogue arrives after MMA j - NACC completed.
@@ -171,7 +178,7 @@ struct Q2Tc {
   __device__ static int raw_row(int r) { return (r >> 5) * 31 + (r & 31); }
   static constexpr int kBoxBytes = kRows * 8 * 34;
   static constexpr bool kQ2 = true;
-  static constexpr int kRawEmptyCount = 8;       // both converter sets
+  static constexpr int kRawEmptyCount = 4 * kConvSets;   // every converter set
   __device__ static void issue_raw(const CUtensorMap* m, uint32_t dst, int g0, int n0, uint32_t bar,
                                    uint64_t pol) {
     tma_load_2d_hint(dst, m, g0 * 17, n0, bar, pol);              // 17 u16 per block
@@ -221,7 +228,7 @@ struct Layout {
   static constexpr int kSclOff = kBOff + SB * kBBytes;
   static constexpr int kBytes = kSclOff + (F::kQ2 ? NSC * BM * 4 : 0);
   static constexpr int kAlloc = kBytes + 1024;                     // slack for 1024-byte alignment
-  static_assert(BM * BN * 4 <= F::kSR * F::kRawBytes, "split-K partials alias the raw ring");
+  static_assert(kEpiSets * BM * BN * 4 <= F::kSR * F::kRawBytes, "split-K partials alias the raw ring");
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
@@ -368,69 +375,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
   }
   const uint32_t tmem = (warp == kTmaWarp) ? 0u : tmem_base_sh;
-  // Partial sums [NB][BM] for the final reduction alias the raw ring: the
-  // epilogue writes them after the MMA of the last group completed, so every
-  // raw stage has been consumed by then.
+  // Partial sums [kEpiSets][NB][BM] for the final reduction alias the raw
+  // ring: an epilogue set writes them only after the MMAs of the last two
+  // groups (one per MMA warp) completed, so every raw stage has been consumed
+  // by then.
   float* red = reinterpret_cast<float*>(smem + L::kRawOff);
 
-  if (warp == kMmaWarp) {
+  if (warp >= kMmaWarp && warp < kMmaWarp + kMmaWarps) {
     // ------------------------------------------------------------ MMA
     constexpr uint32_t idesc = idesc_bf16(BM, BN);
     const uint32_t b_base = sbase + L::kBOff;
-    int issued = 0;
-    for (int j = 0; j < ng; ++j) {
-      const bool ok = wait_or_abort(bar(bars, B::kGo + j % ND), (j / ND) & 1, p.err, abort_flag);
+    int issued = -1;
+    // A wait costs the MMA warp a fixed stall (it resumes only once the
+    // tensor core has taken its earlier MMAs), so it waits for kMmaBatch
+    // groups at a time. Nothing a later group needs depends on an earlier
+    // group's MMA, so waiting ahead cannot deadlock.
+    for (int j0 = (warp - kMmaWarp) * kMmaBatch; j0 < ng; j0 += kMmaWarps * kMmaBatch) {
+      const int j1 = min(j0 + kMmaBatch, ng);
+      bool ok = true;
+      for (int j = j0; j < j1 && ok; ++j) ok = wait_or_abort(bar(bars, B::kGo + j % ND), (j / ND) & 1, p.err, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
       if (elect_one()) {
-        // B: two 128-byte-swizzled boxes of 64 K (2 KB apart), 32 B per
-        // 16-K step, SBO = 1024 B (8-row atoms). The start-address field is
-        // address >> 4, so a step adds 2 and a box adds 128 (no carry:
-        // shared addresses stay below 2^18).
-        const uint64_t bd0 = sdesc(b_base + (j % SB) * kBBytes, 16, 1024, 2);
-        const uint32_t a0 = tmem + (j % SO) * 64;
-        const uint32_t dcol = tmem + kAccCol + (j % NACC) * 16;
+        for (int j = j0; j < j1; ++j) {
+          // B: two 128-byte-swizzled boxes of 64 K (2 KB apart), 32 B per
+          // 16-K step, SBO = 1024 B (8-row atoms). The start-address field
+          // is address >> 4, so a step adds 2 and a box adds 128 (no carry:
+          // shared addresses stay below 2^18).
+          const uint64_t bd0 = sdesc(b_base + (j % SB) * kBBytes, 16, 1024, 2);
+          const uint32_t a0 = tmem + (j % SO) * 64;
+          const uint32_t dcol = tmem + kAccCol + (j % NACC) * 16;
 #pragma unroll
-        for (int i = 0; i < GK / 16; ++i)
-          mma_ts(dcol, a0 + 8 * i, bd0 + static_cast<uint64_t>((i >> 2) * 128 + (i & 3) * 2), idesc,
-                 i > 0 ? 1u : 0u);
-        mma_commit(bar(bars, B::kDone + j % ND));
+          for (int i = 0; i < GK / 16; ++i)
+            mma_ts(dcol, a0 + 8 * i, bd0 + static_cast<uint64_t>((i >> 2) * 128 + (i & 3) * 2), idesc,
+                   i > 0 ? 1u : 0u);
+          mma_commit(bar(bars, B::kDone + j % ND));
+        }
       }
       __syncwarp();
-      issued = j + 1;
+      issued = j1 - 1;
     }
-    // Drain: all MMAs done before TMEM is freed.
-    if (issued > 0) {
-      const int j = issued - 1;
-      mbar_wait(bar(bars, B::kDone + j % ND), (j / ND) & 1, p.err);
-    }
+    // Drain: this warp's MMAs are done before TMEM is freed.
+    if (issued >= 0) mbar_wait(bar(bars, B::kDone + issued % ND), (issued / ND) & 1, p.err);
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ convert
     const int q = warp & 3;                 // TMEM lane quarter = 32-row block
-    const int h = warp >> 2;                // group parity
+    const int h = warp >> 2;                // converter set: groups j = h mod 4
     const int r = q * 32 + lane;
     float* scl = reinterpret_cast<float*>(smem + L::kSclOff);
-    for (int t = (GPR == 1 ? h : 0); t < nst; t += (GPR == 1 ? 2 : 1)) {
+    for (int t = (GPR == 1 ? h : 0); t < nst; t += (GPR == 1 ? kConvSets : 1)) {
       const int sr = t % SR;
       const bool got = wait_or_abort(bar(bars, B::kRawFull + sr), (t / SR) & 1, p.err, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       const uint8_t* raw = smem + L::kRawOff + sr * F::kRawBytes;
       bool live;
 #define WQP_CONV(GI) convert_group<F, GI>(raw, t, q, r, lane, tmem, bars, scl, p.err, abort_flag)
+      static_assert(GPR == 1 || GPR == 2 * kConvSets, "groups of a raw stage per converter set");
       if constexpr (GPR == 1) {
         live = WQP_CONV(0);
       } else if (h == 0) {
-        live = WQP_CONV(0) && WQP_CONV(2) && WQP_CONV(4) && WQP_CONV(6);
+        live = WQP_CONV(0) && WQP_CONV(4);
+      } else if (h == 1) {
+        live = WQP_CONV(1) && WQP_CONV(5);
+      } else if (h == 2) {
+        live = WQP_CONV(2) && WQP_CONV(6);
       } else {
-        live = WQP_CONV(1) && WQP_CONV(3) && WQP_CONV(5) && WQP_CONV(7);
+        live = WQP_CONV(3) && WQP_CONV(7);
       }
 #undef WQP_CONV
       if (!live) break;
       if (lane == 0) mbar_arrive(bar(bars, B::kRawEmpty + sr));
     }
-  } else if (warp < kEpiWarp0 + 4) {
+  } else if (warp < kEpiWarp0 + 4 * kEpiSets) {
     // ------------------------------------------------------------ fold
     const int q = warp & 3;
+    const int es = (warp - kEpiWarp0) >> 2;      // this set folds groups j = es mod 2
     const int r = q * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol;
     const float* scl = reinterpret_cast<const float*>(smem + L::kSclOff);
@@ -438,12 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     float acc[NB];
 #pragma unroll
     for (int m = 0; m < NB; ++m) acc[m] = 0.0f;
-    for (int j = 0; j < ng; ++j) {
+    bool live = true;
+    for (int j = es; j < ng && live; j += kEpiSets) {
       const int sc = j % NACC, nsc = j % NSC;
       bool got = wait_or_abort(bar(bars, B::kDone + j % ND), (j / ND) & 1, p.err, abort_flag);
       if (F::kQ2) got = got && wait_or_abort(bar(bars, B::kSclFull + nsc), (j / NSC) & 1, p.err, abort_flag);
       // Warp-uniform outcome: tcgen05.ld below is .sync.aligned.
-      if (!__all_sync(0xFFFFFFFFu, got)) break;
+      if (!__all_sync(0xFFFFFFFFu, got)) { live = false; break; }
       tc_fence_after();
       float v[NB];
       tmem_ld<NB>(tl + sc * 16, v);
@@ -461,8 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int m = 0; m < NB; ++m) acc[m] = fmaf(v[m], s, acc[m]);
       }
     }
+    for (int g = ng - 2; live && g < ng; ++g) {
+      if (g < 0) continue;
+      live = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(bars, B::kDone + g % ND), (g / ND) & 1, p.err, abort_flag));
+    }
+    if (live) {
 #pragma unroll
-    for (int m = 0; m < NB; ++m) red[m * BM + r] = acc[m];
+      for (int m = 0; m < NB; ++m) red[(es * NB + m) * BM + r] = acc[m];
+    }
   } else if (warp >= kPrepWarp0) {
     // ------------------------------------------------------------ operand hand-off
     // Warp p prepares groups j = p mod 2. Thread (row m, half) rewrites MMA
@@ -509,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------- reduce + store
   __syncthreads();
   const bool failed = *abort_flag != 0;
-  const bool epi = warp >= kEpiWarp0 && warp < kEpiWarp0 + 4;
+  const bool epi = warp >= kEpiWarp0 && warp < kEpiWarp0 + 4;   // the first set stores
   const int er = (warp - kEpiWarp0) * 32 + lane;
   if (splits > 1) cluster_sync();         // every rank's partials are in its shared memory
   if (epi && rank == 0 && !failed && F::raw_row(er) < F::kRows && !(F::kQ2 && (er & 31) == 31)) {
@@ -518,13 +544,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int m = 0; m < NB; ++m) {
       float acc = red[m * BM + er];
+#pragma unroll
+      for (int e = 1; e < kEpiSets; ++e) acc += red[(e * NB + m) * BM + er];
       for (int qq = 1; qq < splits; ++qq) {      // rank order: deterministic
-        float v;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                     : "=f"(v)
-                     : "r"(mapa_shared(mine, qq) + m * BM * 4)
-                     : "memory");
-        acc += v;
+        const uint32_t rem = mapa_shared(mine, qq);
+#pragma unroll
+        for (int e = 0; e < kEpiSets; ++e) {
+          float v;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(rem + (e * NB + m) * BM * 4) : "memory");
+          acc += v;
+        }
       }
       if (m < p.M && n < p.N) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc);
     }
