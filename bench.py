@@ -199,6 +199,8 @@ class Workload:
             wqp.q2_gemm_tc(A, self.W[j], self.N, self.K, out=C)
         elif self.fmt == "q2":
             wqp.q2_gemv(A, self.W[j], self.N, self.K, out=C)
+        elif self.fmt == "w4" and tc:
+            wqp.w4a16_gemm_tc(A, self.W[j], self.S[j], self.N, self.K, out=C)
         elif self.fmt == "w4":
             wqp.w4a16_gemv(A, self.W[j], self.S[j], self.N, self.K, out=C)
         elif tc:
@@ -266,6 +268,7 @@ def sweep(l2, peak):
         ("q2_gemv N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), False, 1),
         ("q2_gemm_tc N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), True, 1),
         ("w4a16_gemv N=5120 K=5120", "w4", 5120, 5120, tuple(range(1, 9)), False, 2),
+        ("w4a16_gemm_tc N=5120 K=5120", "w4", 5120, 5120, (1, 4, 8, 16), True, 2),
         ("w8a16_gemm N=17408 K=5120", "w8", 17408, 5120, (1, 4, 8, 16), False, 3),
         ("w8a16_gemm N=5120 K=17408", "w8", 5120, 17408, (1, 4, 8, 16), False, 3),
         ("w8a16_gemm_tc N=17408 K=5120", "w8", 17408, 5120, (1, 8, 16), True, 3),

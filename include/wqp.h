@@ -77,8 +77,10 @@ int q2_gemv_strided(const void* A, int lda, const void* W, void* C, int ldc,
 
 /* Tensor-core (tcgen05) form of q2_gemv: swap-AB, with the weight rows on
  * the 128-row MMA side and the activation rows padded to 16 on the MMA N
- * side. Every code - 1 is exact in BF16, so the products are exact. Each
- * 128-K group's partial sum is scaled by its inline d once, in FP32.
+ * side. The codes enter the MMA as exact BF16 values c * 4^j * 2^-133 and the
+ * activations as a * 2^(64 - 2j), so every product c * a is exact; each
+ * 128-K group's sum of (c - 1) * a is scaled by its inline d once, in FP32.
+ * Activations must satisfy |a| < 2^62 (the pre-scale stays finite).
  * Arguments and layouts are those of q2_gemv, with two more limits:
  * 1 <= M <= 16, and K % 1024 == 0, so that rows stay 16-byte aligned for the
  * tensor-map copies. Anything else gives WQP_ERR_INVALID_ARG.
@@ -107,6 +109,23 @@ int w4a16_gemv(const void* A, const void* W, const void* scales, void* C,
 int w4a16_gemv_ex(const void* A, int lda, const void* W, const void* scales,
                   float global_scale, void* C, int ldc,
                   int M, int N, int K, void* stream);
+
+/* Tensor-core (tcgen05) form of w4a16_gemv: swap-AB, with the weight rows on
+ * the 128-row MMA side and the activation rows padded to 16 on the MMA N
+ * side. Each e2m1 * e4m3 product is exact in BF16, so the products are
+ * exact; the global scale multiplies each FP32 result once, at the store.
+ * Arguments and layouts are those of w4a16_gemv / w4a16_gemv_ex, with two
+ * more limits: 1 <= M <= 16, and K % 256 == 0, so that the scale rows
+ * (K/16 bytes) are multiples of 16 bytes for the tensor-map copies. Anything
+ * else gives WQP_ERR_INVALID_ARG.
+ * Numerics: the contract is that of w8a16_gemm_tc. It is not bit-identical
+ * to w4a16_gemv. A row does not depend on the other rows of the call.
+ */
+int w4a16_gemm_tc(const void* A, const void* W, const void* scales, void* C,
+                  int M, int N, int K, void* stream);
+int w4a16_gemm_tc_ex(const void* A, int lda, const void* W, const void* scales,
+                     float global_scale, void* C, int ldc,
+                     int M, int N, int K, void* stream);
 
 /* ---------------------------------------------------------------- W8A16 ---
  * FP8 E4M3 weights with FP32 128x128 block scales, scalar-FMA decode GEMM.

@@ -1,4 +1,5 @@
-"""Parity of the tcgen05 swap-AB W8A16 GEMM with the CPU oracle (GPU needed).
+"""Parity of the tcgen05 swap-AB GEMMs (W8A16, Q2_0, W4A16) with the CPU oracle
+(GPU needed).
 
 Tensor-core tolerance ("w8a16_gemm_m16.rs", module docs: within a few BF16
 ULP of the reference or under an absolute floor set by the reduction depth
@@ -36,6 +37,8 @@ def _check_tc(oracle_lib, d, C, what):
     a_rms = np.sqrt((a ** 2).mean(axis=1))
     if d["fmt"] == "q2":
         w_max = np.abs(oracle_lib.q2_dequant(d["W"], d["N"], d["K"])).max(axis=1)
+    elif d["fmt"] == "w4":
+        w_max = np.abs(oracle_lib.w4_dequant(d["W"], d["S"], d.get("g", 1.0), d["N"], d["K"])).max(axis=1)
     else:
         w_max = np.abs(oracle_lib.w8_dequant(d["W"], d["S"], d["N"], d["K"])).max(axis=1)
     ok = tc_ok(C, ref, d["K"], a_rms, w_max)
@@ -129,4 +132,70 @@ def test_q2_tc_full_size(oracle_lib, N, K, Ms):
         d = G.make("q2", M, N, K, seed=synth.seed_for(1, M))
         C = G.host_bits(G.run_gpu(d, tc=True))
         frac = _check_tc(oracle_lib, d, C, f"q2 full M={M} N={N} K={K}")
+        assert frac > 0.99
+
+
+def test_q2_tc_activation_range(oracle_lib):
+    """The pre-scale 2^(64 - 2j) stays exact for large and small activations
+    (|a| up to 2^40 and down to 2^-40), within the stated range."""
+    for scale in (2.0 ** 40, 2.0 ** -40):
+        M, N, K = 4, 300, 2048
+        A = synth.activations(M, K, 77, scale=scale)
+        W, _, _ = synth.q2_weights(N, K, 78)
+        d = {"A": A, "dA": G.dev_bf16(A), "M": M, "N": N, "K": K, "fmt": "q2", "W": W, "dW": G.dev_u8(W)}
+        C = G.host_bits(G.run_gpu(d, tc=True))
+        _check_tc(oracle_lib, d, C, f"q2 activation scale {scale:g}")
+
+
+# ---------------------------------------------------------------- W4A16
+@pytest.mark.parametrize("N,K", [(128, 256), (200, 512), (1000, 1024), (77, 2560), (384, 4096)])
+def test_w4_tc_parity_small(oracle_lib, N, K):
+    for M in (1, 3, 8, 16):
+        d = G.make("w4", M, N, K, seed=700 + N + K + M)
+        C = G.host_bits(G.run_gpu(d, tc=True))
+        _check_tc(oracle_lib, d, C, f"w4 M={M} N={N} K={K}")
+
+
+def test_w4_tc_global_scale(oracle_lib):
+    d = G.make("w4", 5, 300, 1024, seed=31)
+    d["g"] = 0.37109375
+    C = G.host_bits(G.run_gpu(d, tc=True))
+    _check_tc(oracle_lib, d, C, "w4 global scale")
+
+
+def test_w4_tc_exact_arithmetic_bit_exact(oracle_lib):
+    """Integer activations, power-of-two group scales, g = 1: every partial sum
+    is exact, so any summation order gives the oracle's bits."""
+    r = np.random.default_rng(9)
+    M, N, K = 16, 260, 2048
+    A = synth.bf16_bits_from_f32(r.integers(-4, 5, size=(M, K)).astype(np.float32))
+    nib = r.integers(0, 16, size=(N, K), dtype=np.uint8)
+    W = synth.pack_w4(nib)
+    S = synth.e4m3_round(2.0 ** r.integers(-2, 3, size=(N, K // 16)))
+    d = {"A": A, "dA": G.dev_bf16(A), "M": M, "N": N, "K": K, "fmt": "w4", "W": W, "S": S,
+         "dW": G.dev_u8(W), "dS": G.dev_u8(S), "g": 1.0}
+    C = G.host_bits(G.run_gpu(d, tc=True))
+    assert np.array_equal(C, G.run_oracle(oracle_lib, d).c)
+
+
+def test_w4_tc_rows_independent_and_k_rule():
+    import weight_only_quantized_packed_gb300 as wqp
+
+    d = G.make("w4", 16, 5120, 5120, seed=22)
+    c16 = G.host_bits(G.run_gpu(d, tc=True))
+    assert np.array_equal(c16, G.host_bits(G.run_gpu(d, tc=True)))   # deterministic split-K
+    for m in (0, 9, 15):
+        one = G.host_bits(G.run_gpu(d, tc=True, A=d["dA"][m:m + 1]))
+        assert np.array_equal(one[0], c16[m])
+    bad = G.make("w4", 1, 64, 384, seed=3)
+    with pytest.raises(wqp.WqpError):
+        G.run_gpu(bad, tc=True)          # K % 256 != 0
+
+
+@pytest.mark.parametrize("N,K,Ms", [(5120, 5120, (1, 8, 16)), (17408, 5120, (4,))])
+def test_w4_tc_full_size(oracle_lib, N, K, Ms):
+    for M in Ms:
+        d = G.make("w4", M, N, K, seed=synth.seed_for(2, M))
+        C = G.host_bits(G.run_gpu(d, tc=True))
+        frac = _check_tc(oracle_lib, d, C, f"w4 full M={M} N={N} K={K}")
         assert frac > 0.99

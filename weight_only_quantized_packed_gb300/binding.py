@@ -12,7 +12,7 @@ import os
 import threading
 
 __all__ = [
-    "WqpError", "lib", "lib_path", "q2_gemv", "q2_gemm_tc", "w4a16_gemv", "w8a16_gemm", "w8a16_gemm_tc",
+    "WqpError", "lib", "lib_path", "q2_gemv", "q2_gemm_tc", "w4a16_gemv", "w4a16_gemm_tc", "w8a16_gemm", "w8a16_gemm_tc",
     "q2_dequant", "w4a16_dequant", "w8a16_dequant", "row_chunks", "set_pdl",
     "get_device_error", "status_string", "EXPORTS", "MAX_M_PER_LAUNCH",
 ]
@@ -33,6 +33,8 @@ EXPORTS = {
     "q2_gemm_tc_strided": [_P, _I, _P, _P, _I, _I, _I, _I, _P],
     "w4a16_gemv": [_P, _P, _P, _P, _I, _I, _I, _P],
     "w4a16_gemv_ex": [_P, _I, _P, _P, _F, _P, _I, _I, _I, _I, _P],
+    "w4a16_gemm_tc": [_P, _P, _P, _P, _I, _I, _I, _P],
+    "w4a16_gemm_tc_ex": [_P, _I, _P, _P, _F, _P, _I, _I, _I, _I, _P],
     "w8a16_gemm": [_P, _P, _P, _P, _I, _I, _I, _P],
     "w8a16_gemm_strided": [_P, _I, _P, _P, _P, _I, _I, _I, _I, _P],
     "w8a16_gemm_tc": [_P, _P, _P, _P, _I, _I, _I, _P],
@@ -151,6 +153,16 @@ def w4a16_gemv(A, W, scales, N: int, K: int, global_scale: float = 1.0, out=None
     C = _out(A, M, N, out)
     _check(lib().w4a16_gemv_ex(_ptr(A), lda, _ptr(W), _ptr(scales), float(global_scale), _ptr(C),
                                C.stride(0), M, N, K, _stream(stream)), "w4a16_gemv")
+    return C
+
+
+def w4a16_gemm_tc(A, W, scales, N: int, K: int, global_scale: float = 1.0, out=None, stream=None):
+    """Tensor-core (tcgen05 swap-AB) form of w4a16_gemv, 1 <= M <= 16, K % 256 == 0."""
+    _need_cuda(A, W, scales, out)
+    M, lda = _rows(A, K)
+    C = _out(A, M, N, out)
+    _check(lib().w4a16_gemm_tc_ex(_ptr(A), lda, _ptr(W), _ptr(scales), float(global_scale), _ptr(C),
+                                  C.stride(0), M, N, K, _stream(stream)), "w4a16_gemm_tc")
     return C
 
 

@@ -80,7 +80,7 @@ int device_setup(DeviceInfo** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-enum class Fmt { Q2, W4, W8, W8TC, Q2TC };
+enum class Fmt { Q2, W4, W8, W8TC, Q2TC, W4TC };
 
 const char* fmt_name(Fmt f) {
   switch (f) {
@@ -89,6 +89,7 @@ const char* fmt_name(Fmt f) {
     case Fmt::W8: return "w8a16_gemm";
     case Fmt::W8TC: return "w8a16_gemm_tc";
     case Fmt::Q2TC: return "q2_gemm_tc";
+    case Fmt::W4TC: return "w4a16_gemm_tc";
   }
   return "?";
 }
@@ -97,7 +98,8 @@ int validate(Fmt f, const void* A, int lda, const void* W, const void* scales, v
              int M, int N, int K) {
   const char* nm = fmt_name(f);
   if (M < 0) return fail(WQP_ERR_INVALID_ARG, "%s: M=%d < 0", nm, M);
-  const bool tc = (f == Fmt::W8TC || f == Fmt::Q2TC);
+  const bool tc = (f == Fmt::W8TC || f == Fmt::Q2TC || f == Fmt::W4TC);
+  const bool w4 = (f == Fmt::W4 || f == Fmt::W4TC);
   const bool q2 = (f == Fmt::Q2 || f == Fmt::Q2TC);
   if (tc && (M < 1 || M > 16))
     return fail(WQP_ERR_INVALID_ARG, "%s: M=%d outside 1..16 (kernel M tile)", nm, M);
@@ -107,12 +109,14 @@ int validate(Fmt f, const void* A, int lda, const void* W, const void* scales, v
   if (!A || !W || !C) return fail(WQP_ERR_INVALID_ARG, "%s: NULL A, W or C", nm);
   if (f == Fmt::Q2TC && K % 1024 != 0)
     return fail(WQP_ERR_INVALID_ARG, "%s: K=%d must be a multiple of 1024", nm, K);
+  if (f == Fmt::W4TC && K % 256 != 0)
+    return fail(WQP_ERR_INVALID_ARG, "%s: K=%d must be a multiple of 256", nm, K);
   if (q2 && scales)
     return fail(WQP_ERR_INVALID_ARG, "%s: Q2_0 scales are inline; scales must be NULL", nm);
   if (!q2 && !scales) return fail(WQP_ERR_INVALID_ARG, "%s: NULL scales", nm);
   if (!aligned(A, 16) || !aligned(W, 16))
     return fail(WQP_ERR_INVALID_ARG, "%s: A and W must be 16-byte aligned", nm);
-  if (f == Fmt::W4 && !aligned(scales, 16))
+  if (w4 && !aligned(scales, 16))
     return fail(WQP_ERR_INVALID_ARG, "%s: scales must be 16-byte aligned", nm);
   if ((f == Fmt::W8 || f == Fmt::W8TC) && !aligned(scales, 4))
     return fail(WQP_ERR_INVALID_ARG, "%s: scales must be 4-byte aligned", nm);
@@ -127,8 +131,8 @@ int run_gemm(Fmt f, const void* A, int lda, const void* W, const void* scales, f
              void* C, int ldc, int M, int N, int K, void* stream) {
   int st = validate(f, A, lda, W, scales, C, ldc, M, N, K);
   if (st != WQP_OK) return st;
-  if (f == Fmt::W4 && !(gscale == gscale))
-    return fail(WQP_ERR_INVALID_ARG, "w4a16_gemv: global_scale is NaN");
+  if ((f == Fmt::W4 || f == Fmt::W4TC) && !(gscale == gscale))
+    return fail(WQP_ERR_INVALID_ARG, "%s: global_scale is NaN", fmt_name(f));
   if (M == 0) return WQP_OK;
   DeviceInfo* dev = nullptr;
   if ((st = device_setup(&dev)) != WQP_OK) return st;
@@ -156,6 +160,7 @@ int run_gemm(Fmt f, const void* A, int lda, const void* W, const void* scales, f
       case Fmt::W8: e = launch_w8a16_gemm(a, s); break;
       case Fmt::W8TC: e = launch_w8a16_gemm_tc(a, s); break;
       case Fmt::Q2TC: e = launch_q2_gemm_tc(a, s); break;
+      case Fmt::W4TC: e = launch_w4a16_gemm_tc(a, s); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, fmt_name(f));
   }
@@ -222,6 +227,16 @@ int w4a16_gemv(const void* A, const void* W, const void* scales, void* C, int M,
 int w4a16_gemv_ex(const void* A, int lda, const void* W, const void* scales, float global_scale,
                   void* C, int ldc, int M, int N, int K, void* stream) {
   return run_gemm(Fmt::W4, A, lda, W, scales, global_scale, C, ldc, M, N, K, stream);
+}
+
+int w4a16_gemm_tc(const void* A, const void* W, const void* scales, void* C, int M, int N, int K,
+                  void* stream) {
+  return run_gemm(Fmt::W4TC, A, K, W, scales, 1.0f, C, N, M, N, K, stream);
+}
+
+int w4a16_gemm_tc_ex(const void* A, int lda, const void* W, const void* scales, float global_scale,
+                     void* C, int ldc, int M, int N, int K, void* stream) {
+  return run_gemm(Fmt::W4TC, A, lda, W, scales, global_scale, C, ldc, M, N, K, stream);
 }
 
 int w8a16_gemm(const void* A, const void* W, const float* scales, void* C, int M, int N, int K,

@@ -1,5 +1,7 @@
 // Tensor-core (tcgen05) swap-AB decode GEMM for packed weights, 1 <= M <= 16.
 //
+// W4 (E2M1 codes, E4M3 scale per 16 K, FP32 per-tensor scale;
+// "spark_model/layers/w4a16_gemv_tiers.rs", module docs),
 // FP8 E4M3 with FP32 128x128 block scales
 // ("metrale_model_layers/layers/ops/w8a16_gemm_m16.rs": doc of
 // `w8a16_gemm_m16` for the operands and the 16-row M tile; module docs for
@@ -20,6 +22,10 @@
 //
 // Encodings (every product is exact in FP32):
 //  * FP8: each E4M3 value is a BF16 value; B is the activation tile as loaded.
+//  * W4: e2m1 * e4m3 scale has at most 6 significant bits and lies in
+//    [2^-10, 2688], so it is exact in FP16 and in BF16; the per-tensor scale
+//    multiplies the FP32 result once, at the store. B is the activation tile
+//    as loaded.
 //  * Q2_0: the two codes (c_j, c_{j+8}) of a 16-code word sit at bits (2j,
 //    2j+16). Masking them in place (one LOP3 per pair) gives two BF16
 //    subnormals c * 4^(j mod 4) * 2^-133 (exact: the field stays below the
@@ -110,7 +116,8 @@ static_assert(kMmaBatch <= NACC && kMmaBatch <= SO, "the MMA warp waits for a ba
 constexpr int kBBytes = BN * GK * 2;   // 4 KB: two [16 rows x 64 K] boxes, 128-byte swizzle
 
 struct TcParams {
-  const float* scales;     // FP8: [ceil(N/128), K/128]; Q2_0: unused
+  const float* scales;     // FP8: [ceil(N/128), K/128]; Q2_0, W4: unused here
+  float gscale;            // W4 per-tensor scale (1 otherwise)
   uint16_t* C;
   int M, N, K, ldc;
   int splits;              // CTAs per tile (cluster size)
@@ -135,9 +142,9 @@ struct Fp8Tc {
   static constexpr int kRawBytes = BM * GK;      // stage stride
   static constexpr int kBoxBytes = kRows * GK;   // bytes one stage load delivers
   static constexpr bool kQ2 = false;
-  static constexpr int kRawEmptyCount = 4;       // one converter set per stage
-  __device__ static void issue_raw(const CUtensorMap* m, uint32_t dst, int g0, int n0, uint32_t bar,
-                                   uint64_t pol) {
+  static constexpr bool kBlockScale = true;      // fold s[n/128, g] per group
+  __device__ static void issue_raw(const CUtensorMap* m, const CUtensorMap*, uint32_t dst, int g0, int n0,
+                                   uint32_t bar, uint64_t pol) {
     tma_load_2d_hint(dst, m, g0 * GK, n0, bar, pol);
   }
   // TMEM lane r = weight row r of the tile.
@@ -178,9 +185,9 @@ struct Q2Tc {
   __device__ static int raw_row(int r) { return (r >> 5) * 31 + (r & 31); }
   static constexpr int kBoxBytes = kRows * 8 * 34;
   static constexpr bool kQ2 = true;
-  static constexpr int kRawEmptyCount = 4 * kConvSets;   // every converter set
-  __device__ static void issue_raw(const CUtensorMap* m, uint32_t dst, int g0, int n0, uint32_t bar,
-                                   uint64_t pol) {
+  static constexpr bool kBlockScale = false;
+  __device__ static void issue_raw(const CUtensorMap* m, const CUtensorMap*, uint32_t dst, int g0, int n0,
+                                   uint32_t bar, uint64_t pol) {
     tma_load_2d_hint(dst, m, g0 * 17, n0, bar, pol);              // 17 u16 per block
   }
   // Block GI of row r: its 34 bytes start OFF = 34 GI mod 16 bytes into a
@@ -218,6 +225,62 @@ struct Q2Tc {
     constexpr int dw = (off + 32) / 4;
     const uint32_t dbits = (off % 4 == 0) ? (wv[dw] & 0xFFFFu) : (wv[dw] >> 16);
     d = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+  }
+};
+
+// W4: two groups per raw stage: codes [128 rows x 128 B] with the 128-byte
+// swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)), then the E4M3
+// scales [128 rows x 16 B]. Group gi of the stage is code chunks 4 gi .. 4 gi + 3
+// and scale bytes 8 gi .. 8 gi + 7 of the row.
+struct W4Tc {
+  static constexpr int kRows = 128;
+  static constexpr int kGPR = 2;
+  static constexpr int kSR = 8;
+  static constexpr int kCodeBytes = BM * 128;
+  static constexpr int kRawBytes = kCodeBytes + BM * 16;   // stage stride (1024-multiple)
+  static constexpr int kBoxBytes = kRawBytes;
+  static constexpr bool kQ2 = false;
+  static constexpr bool kBlockScale = false;
+  static_assert(kRawBytes % 1024 == 0, "raw stages keep the swizzle atoms aligned");
+  __device__ static void issue_raw(const CUtensorMap* m, const CUtensorMap* m2, uint32_t dst, int g0,
+                                   int n0, uint32_t bar, uint64_t pol) {
+    tma_load_2d_hint(dst, m, g0 * (GK / 2), n0, bar, pol);                // code bytes
+    tma_load_2d_hint(dst + kCodeBytes, m2, g0 * (GK / 16), n0, bar, pol); // scale bytes
+  }
+  __device__ static int raw_row(int r) { return r; }
+  // Row r, group GI of the stage -> 64 TMEM columns from tcol: 16-K step i is
+  // code bytes 8i..8i+7 of the group and scale byte i; natural pairs
+  // (16i + 2b, 16i + 2b + 1) = byte b in column 8i + b.
+  template <int GI>
+  __device__ static void convert(const uint8_t* raw, int r, uint32_t tcol, float& d) {
+    const uint8_t* row = raw + r * 128;
+    const uint2 sc = *reinterpret_cast<const uint2*>(raw + kCodeBytes + r * 16 + GI * 8);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {                              // one code chunk = steps 2h, 2h+1
+      const int c = 4 * GI + h;
+      const uint4 x = lds128(row + ((c ^ (r & 7)) << 4));
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+      uint32_t v[16];
+#pragma unroll
+      for (int st = 0; st < 2; ++st) {
+        const int step = 2 * h + st;
+        const uint32_t sbyte = ((step < 4 ? sc.x : sc.y) >> (8 * (step & 3))) & 0xFFu;
+        const uint32_t s16 = e4m3x2_to_f16x2(sbyte) & 0xFFFFu;
+        const uint32_t s2 = s16 | (s16 << 16);                 // {s, s} as f16x2
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t word = xs[2 * st + w];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            uint32_t hp = e2m1x2_to_f16x2((word >> (8 * b)) & 0xFFu);
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hp) : "r"(hp), "r"(s2));
+            v[8 * st + 4 * w + b] = f16x2_to_bf16x2_exact(hp);
+          }
+        }
+      }
+      tmem_st16(tcol + 16 * h, v);
+    }
+    d = 1.0f;
   }
 };
 
@@ -276,8 +339,8 @@ __device__ __forceinline__ bool convert_group(const uint8_t* raw, int t, int q, 
 
 template <class F, int NB>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
-              TcParams p) {
+    tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
+              const __grid_constant__ CUtensorMap tmA, TcParams p) {
   using L = Layout<F>;
   constexpr int SR = F::kSR;
   constexpr int GPR = F::kGPR;
@@ -306,7 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < B::kCount; ++i) {
       uint32_t count = 1;
-      if (i >= B::kRawEmpty && i < B::kBLoad) count = F::kRawEmptyCount;
+      // Converter warps that release a raw stage: the sets owning its groups.
+      if (i >= B::kRawEmpty && i < B::kBLoad) count = 4 * (GPR < kConvSets ? GPR : kConvSets);
       if (i >= B::kGo && i < B::kDone) count = kGoCount;
       if (i >= B::kSclFull) count = 4;
       mbar_init(bar(bars, i), count);
@@ -327,13 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // they start before griddepcontrol.wait); lane 1 streams activation tiles.
     if (lane == 0) {
       prefetch_tmap(&tmW);
+      if (F::kGPR == 2) prefetch_tmap(&tmW2);
       const uint64_t pol = policy_evict_first();
       int raw_issued = 0;
       for (int t = 0; t < nst; ++t) {
         const int sr = t % SR;
         if (t >= SR && !wait_or_abort(bar(bars, B::kRawEmpty + sr), ((t / SR) - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(bar(bars, B::kRawFull + sr), F::kBoxBytes);
-        F::issue_raw(&tmW, sbase + L::kRawOff + sr * F::kRawBytes, g_begin + t * GPR, n0,
+        F::issue_raw(&tmW, &tmW2, sbase + L::kRawOff + sr * F::kRawBytes, g_begin + t * GPR, n0,
                      bar(bars, B::kRawFull + sr), pol);
         raw_issued = t + 1;
       }
@@ -423,16 +488,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp >> 2;                // converter set: groups j = h mod 4
     const int r = q * 32 + lane;
     float* scl = reinterpret_cast<float*>(smem + L::kSclOff);
-    for (int t = (GPR == 1 ? h : 0); t < nst; t += (GPR == 1 ? kConvSets : 1)) {
+    // Set h converts the groups j = h mod 4: with one group per raw stage the
+    // stages t = h mod 4, with two the group h % 2 of stages t = h / 2 mod 2,
+    // with eight the groups h and h + 4 of every stage.
+    const int t0 = GPR == 1 ? h : (GPR == 2 ? (h >> 1) : 0);
+    const int dt = GPR == 1 ? kConvSets : (GPR == 2 ? 2 : 1);
+    for (int t = t0; t < nst; t += dt) {
       const int sr = t % SR;
       const bool got = wait_or_abort(bar(bars, B::kRawFull + sr), (t / SR) & 1, p.err, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       const uint8_t* raw = smem + L::kRawOff + sr * F::kRawBytes;
       bool live;
 #define WQP_CONV(GI) convert_group<F, GI>(raw, t, q, r, lane, tmem, bars, scl, p.err, abort_flag)
-      static_assert(GPR == 1 || GPR == 2 * kConvSets, "groups of a raw stage per converter set");
+      static_assert(GPR == 1 || GPR == 2 || GPR == 2 * kConvSets, "groups of a raw stage per converter set");
       if constexpr (GPR == 1) {
         live = WQP_CONV(0);
+      } else if constexpr (GPR == 2) {
+        live = (h & 1) ? WQP_CONV(1) : WQP_CONV(0);
       } else if (h == 0) {
         live = WQP_CONV(0) && WQP_CONV(4);
       } else if (h == 1) {
@@ -453,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol;
     const float* scl = reinterpret_cast<const float*>(smem + L::kSclOff);
-    const float* srow = F::kQ2 ? nullptr : p.scales + static_cast<size_t>(tile) * (p.K / GK);
+    const float* srow = F::kBlockScale ? p.scales + static_cast<size_t>(tile) * (p.K / GK) : nullptr;
     float acc[NB];
 #pragma unroll
     for (int m = 0; m < NB; ++m) acc[m] = 0.0f;
@@ -475,10 +547,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float d69 = scl[nsc * BM + r] * 0x1p69f;
 #pragma unroll
         for (int m = 0; m < NB; ++m) acc[m] = fmaf(d69, v[m] - __shfl_sync(0xFFFFFFFFu, v[m], 31), acc[m]);
-      } else {
+      } else if (F::kBlockScale) {
         const float s = __ldg(srow + g_begin + j);
 #pragma unroll
         for (int m = 0; m < NB; ++m) acc[m] = fmaf(v[m], s, acc[m]);
+      } else {
+#pragma unroll
+        for (int m = 0; m < NB; ++m) acc[m] += v[m];
       }
     }
     for (int g = ng - 2; live && g < ng; ++g) {
@@ -555,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc += v;
         }
       }
-      if (m < p.M && n < p.N) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc);
+      if (m < p.M && n < p.N) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc * p.gscale);
     }
   }
   if (splits > 1) cluster_sync();         // remote partials stay alive until read
@@ -579,7 +654,8 @@ int choose_splits(int tiles, int stages, int num_sms) {
 }
 
 template <class F, int NB>
-cudaError_t launch_tc_nb(const CUtensorMap& mw, const CUtensorMap& ma, const TcParams& p, int tiles, bool pdl,
+cudaError_t launch_tc_nb(const CUtensorMap& mw, const CUtensorMap& mw2, const CUtensorMap& ma, const TcParams& p,
+                         int tiles, bool pdl,
                          cudaStream_t s) {
   using L = Layout<F>;
   static bool attr_set = false;
@@ -611,11 +687,11 @@ cudaError_t launch_tc_nb(const CUtensorMap& mw, const CUtensorMap& ma, const TcP
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, tc_kernel<F, NB>, mw, ma, p);
+  return cudaLaunchKernelEx(&cfg, tc_kernel<F, NB>, mw, mw2, ma, p);
 }
 
 template <class F>
-cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, cudaStream_t s) {
+cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, const CUtensorMap& mw2, cudaStream_t s) {
   CUtensorMap ma;
   cudaError_t e = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, static_cast<uint64_t>(a.K),
                               static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda) * 2, 64, BN,
@@ -624,6 +700,7 @@ cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, cudaStream_t s) 
   const int tiles = (a.N + F::kRows - 1) / F::kRows;
   TcParams p;
   p.scales = static_cast<const float*>(a.scales);
+  p.gscale = a.gscale;
   p.C = static_cast<uint16_t*>(a.C);
   p.M = a.M;
   p.N = a.N;
@@ -632,11 +709,11 @@ cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, cudaStream_t s) 
   p.stages = a.K / (GK * F::kGPR);
   p.splits = choose_splits(tiles, p.stages, a.num_sms);
   p.err = a.err;
-  if (a.M <= 1) return launch_tc_nb<F, 1>(mw, ma, p, tiles, a.pdl, s);
-  if (a.M <= 2) return launch_tc_nb<F, 2>(mw, ma, p, tiles, a.pdl, s);
-  if (a.M <= 4) return launch_tc_nb<F, 4>(mw, ma, p, tiles, a.pdl, s);
-  if (a.M <= 8) return launch_tc_nb<F, 8>(mw, ma, p, tiles, a.pdl, s);
-  return launch_tc_nb<F, 16>(mw, ma, p, tiles, a.pdl, s);
+  if (a.M <= 1) return launch_tc_nb<F, 1>(mw, mw2, ma, p, tiles, a.pdl, s);
+  if (a.M <= 2) return launch_tc_nb<F, 2>(mw, mw2, ma, p, tiles, a.pdl, s);
+  if (a.M <= 4) return launch_tc_nb<F, 4>(mw, mw2, ma, p, tiles, a.pdl, s);
+  if (a.M <= 8) return launch_tc_nb<F, 8>(mw, mw2, ma, p, tiles, a.pdl, s);
+  return launch_tc_nb<F, 16>(mw, mw2, ma, p, tiles, a.pdl, s);
 }
 
 }  // namespace tc
@@ -648,7 +725,7 @@ cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s) {
                               static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K), GK, BM,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  return launch_tc<Fp8Tc>(a, mw, s);
+  return launch_tc<Fp8Tc>(a, mw, mw, s);
 }
 
 // Requires K % 1024 == 0 (checked by the caller): a row is then 34 * K / 128
@@ -661,7 +738,23 @@ cudaError_t launch_q2_gemm_tc(const GemvArgs& a, cudaStream_t s) {
   cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),
                               34 * G, 8 * 17, Q2Tc::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  return launch_tc<Q2Tc>(a, mw, s);
+  return launch_tc<Q2Tc>(a, mw, mw, s);
+}
+
+// Requires K % 256 == 0 (checked by the caller): the scale rows (K/16 bytes)
+// are then a multiple of 16 bytes, as tensor maps need, and every raw stage
+// holds two whole groups.
+cudaError_t launch_w4a16_gemm_tc(const GemvArgs& a, cudaStream_t s) {
+  using namespace tc;
+  const uint64_t K = static_cast<uint64_t>(a.K);
+  CUtensorMap mw, ms;
+  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, K / 2, static_cast<uint64_t>(a.N), K / 2,
+                              128, W4Tc::kRows, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  e = make_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, K / 16, static_cast<uint64_t>(a.N), K / 16, 16,
+                  W4Tc::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  return launch_tc<W4Tc>(a, mw, ms, s);
 }
 
 }  // namespace wqp
