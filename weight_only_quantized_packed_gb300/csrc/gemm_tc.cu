@@ -50,13 +50,14 @@
 //          tcgen05.ld of the group's accumulator slot (lane = weight row,
 //          column = activation row) and the FP32 fold; each set keeps its own
 //          partial sums, added in a fixed order at the end;
-//   24     TMA: lane 0 raw weight stages, lane 1 activation tiles;
+//   24     TMA of the raw weight stages (lane 0);
 //   25..26 MMA (alternate groups; 25 allocates TMEM): per group one wait,
 //          then the elected lane issues the 8 MMAs into the group's
 //          accumulator slot and commits once ("MMA of group j done");
 //   27..28 activation operand hand-off (alternate groups): Q2_0 tiles are
 //          prepared in place on the tile the TMA loaded; FP8 tiles are used
-//          as loaded.
+//          as loaded;
+//   29     TMA of the activation tiles (lane 0).
 // The MMA warp waits on a single barrier per group, "group j may start",
 // which completes after nine arrivals: the four converter warps of the set,
 // the activation operand (its hand-off warp) and
@@ -90,13 +91,15 @@ constexpr int kMmaWarps = 2;
 constexpr int kMmaBatch = 1;       // groups issued per wait of the MMA warp
 constexpr int kPrepWarp0 = 27;     // activation hand-off warps 27..28
 constexpr int kPrepWarps = 2;
-constexpr int kThreads = 29 * 32;
+constexpr int kActWarp = 29;       // activation TMA (its own warp: divergent lanes of one warp
+                                   // that wait on different barriers delay each other)
+constexpr int kThreads = 30 * 32;
 constexpr int SO = 6;              // TMEM operand stages, one group (64 columns) each
 constexpr int NACC = 8;            // TMEM accumulator slots, 16 columns each
 constexpr uint32_t kAccCol = SO * 64;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kAccCol + NACC * 16 <= kTmemCols, "TMEM budget");
-constexpr int SB = 8;              // activation operand stages
+constexpr int SB = 16;             // activation operand stages (a CTA of <= 16 groups loads them all at once)
 constexpr int ND = 16;             // "MMA of group j done" and "group j may start" rings
 constexpr int kGoCount = 4 + 1 + 4;   // converter warps + operand + epilogue warps
 constexpr int NSC = 16;            // per-group row-scale ring (converters -> epilogue)
@@ -113,7 +116,14 @@ static_assert(kMmaBatch <= NACC && kMmaBatch <= SO, "the MMA warp waits for a ba
 // "Group j may start" slot j % ND receives arrivals for group j only after the
 // MMA of group j - ND was issued: converters wait for MMA j - SO, the operand
 // producer for MMA j - SB, the epilogue arrives after MMA j - NACC completed.
-constexpr int kBBytes = BN * GK * 2;   // 4 KB: two [16 rows x 64 K] boxes, 128-byte swizzle
+// Activation slot: two [16 rows x 64 K] boxes (2 KB apart), 128-byte swizzle.
+// The TMA fills rows 0 .. NB-1 of each box (NB = M rounded up to a power of
+// two, rows >= M zero-filled); rows NB..15 are never loaded and only reach
+// accumulator columns >= NB, which nothing reads.
+constexpr int kBBytes = BN * GK * 2;
+// Split-K partial sums pushed to the owning rank: [splits][NB][rows per rank],
+// at most 16 x (8 x 16 + 8) floats.
+constexpr int kRecvBytes = BN * (BM + 8) * 4;
 
 struct TcParams {
   const float* scales;     // FP8: [ceil(N/128), K/128]; Q2_0, W4: unused here
@@ -289,7 +299,8 @@ struct Layout {
   static constexpr int kRawOff = 0;
   static constexpr int kBOff = (kRawOff + F::kSR * F::kRawBytes + 1023) / 1024 * 1024;
   static constexpr int kSclOff = kBOff + SB * kBBytes;
-  static constexpr int kBytes = kSclOff + (F::kQ2 ? NSC * BM * 4 : 0);
+  static constexpr int kRecvOff = kSclOff + (F::kQ2 ? NSC * BM * 4 : 0);
+  static constexpr int kBytes = kRecvOff + kRecvBytes;
   static constexpr int kAlloc = kBytes + 1024;                     // slack for 1024-byte alignment
   static_assert(kEpiSets * BM * BN * 4 <= F::kSR * F::kRawBytes, "split-K partials alias the raw ring");
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -385,15 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   pdl_launch_dependents();
 
-  if (warp == kTmaWarp) {
+  int raw_issued = 0, act_issued = 0;     // copies issued by lane 0 of the TMA / activation warp
+  if (warp == kTmaWarp || warp == kActWarp) {
     // ------------------------------------------------------------ TMA
-    // Lane 0 streams raw weight stages (independent of the previous grid, so
-    // they start before griddepcontrol.wait); lane 1 streams activation tiles.
-    if (lane == 0) {
+    // Lane 0 of the TMA warp streams raw weight stages (independent of the
+    // previous grid, so they start before griddepcontrol.wait); lane 0 of the
+    // activation warp streams activation tiles.
+    if (warp == kTmaWarp && lane == 0) {
       prefetch_tmap(&tmW);
       if (F::kGPR == 2) prefetch_tmap(&tmW2);
       const uint64_t pol = policy_evict_first();
-      int raw_issued = 0;
       for (int t = 0; t < nst; ++t) {
         const int sr = t % SR;
         if (t >= SR && !wait_or_abort(bar(bars, B::kRawEmpty + sr), ((t / SR) - 1) & 1, p.err, abort_flag)) break;
@@ -402,16 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                      bar(bars, B::kRawFull + sr), pol);
         raw_issued = t + 1;
       }
-      // Drain: every issued copy has landed before the CTA may exit.
-      for (int t = max(0, raw_issued - SR); t < raw_issued; ++t)
-        mbar_wait(bar(bars, B::kRawFull + t % SR), (t / SR) & 1, p.err);
-    } else if (lane == 1) {
-      // Activation tiles [16 rows x 128 K] (rows >= M zero-filled) into the
+    } else if (warp == kActWarp && lane == 0) {
+      // Activation tiles [NB rows x 128 K] (rows >= M zero-filled) into the
       // operand ring; Q2_0 tiles are rewritten in place by the preparation
       // warps before the MMA reads them.
       prefetch_tmap(&tmA);
       pdl_wait();                          // activations may come from the previous grid
-      int issued = 0;
       for (int j = 0; j < ng; ++j) {
         const int s = j % SB;
         const int full = B::kBLoad + s;
@@ -419,16 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int g = j - SB;            // previous user of the stage
           if (!wait_or_abort(bar(bars, B::kDone + g % ND), (g / ND) & 1, p.err, abort_flag)) break;
         }
-        mbar_arrive_expect_tx(bar(bars, full), kBBytes);
+        mbar_arrive_expect_tx(bar(bars, full), NB * GK * 2);
         const uint32_t dst = sbase + L::kBOff + s * kBBytes;
         tma_load_2d(dst, &tmA, (g_begin + j) * GK, 0, bar(bars, full));
         tma_load_2d(dst + kBBytes / 2, &tmA, (g_begin + j) * GK + 64, 0, bar(bars, full));
-        issued = j + 1;
+        act_issued = j + 1;
       }
-      // Drain: every issued copy has landed before the CTA may exit.
-      for (int j = max(0, issued - SB); j < issued; ++j)
-        mbar_wait(bar(bars, B::kBLoad + j % SB), (j / SB) & 1, p.err);
     }
+    __syncwarp();                          // the CTA barriers below need a converged warp
   } else {
     // Everyone else needs the TMEM base address.
     if (warp == kMmaWarp) {
@@ -436,10 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_relinquish();
       tc_fence_before();
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 64) : "memory");
     tc_fence_after();
   }
-  const uint32_t tmem = (warp == kTmaWarp) ? 0u : tmem_base_sh;
+  const uint32_t tmem = (warp == kTmaWarp || warp == kActWarp) ? 0u : tmem_base_sh;
   // Partial sums [kEpiSets][NB][BM] for the final reduction alias the raw
   // ring: an epilogue set writes them only after the MMAs of the last two
   // groups (one per MMA warp) completed, so every raw stage has been consumed
@@ -564,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < NB; ++m) red[(es * NB + m) * BM + r] = acc[m];
     }
-  } else if (warp >= kPrepWarp0) {
+  } else if (warp >= kPrepWarp0 && warp < kPrepWarp0 + kPrepWarps) {
     // ------------------------------------------------------------ operand hand-off
     // Warp p prepares groups j = p mod 2. Thread (row m, half) rewrites MMA
     // steps 4 half .. 4 half + 3 in place: the natural chunks
@@ -608,36 +614,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------------------------------------------------- reduce + store
+  // Rank q of the cluster owns tile rows [q R, q R + R), R = ceil(BM / splits).
+  // Every rank adds its two epilogue sets' partials and pushes them into the
+  // owner's receive area (slot = source rank); after one cluster barrier each
+  // owner adds the slots in rank order and stores its rows. The order of the
+  // additions depends only on N and K, never on M.
   __syncthreads();
-  const bool failed = *abort_flag != 0;
-  const bool epi = warp >= kEpiWarp0 && warp < kEpiWarp0 + 4;   // the first set stores
-  const int er = (warp - kEpiWarp0) * 32 + lane;
-  if (splits > 1) cluster_sync();         // every rank's partials are in its shared memory
-  if (epi && rank == 0 && !failed && F::raw_row(er) < F::kRows && !(F::kQ2 && (er & 31) == 31)) {
-    const int n = n0 + F::raw_row(er);
-    const uint32_t mine = smem_u32(red + er);
-#pragma unroll
-    for (int m = 0; m < NB; ++m) {
-      float acc = red[m * BM + er];
-#pragma unroll
-      for (int e = 1; e < kEpiSets; ++e) acc += red[(e * NB + m) * BM + er];
-      for (int qq = 1; qq < splits; ++qq) {      // rank order: deterministic
-        const uint32_t rem = mapa_shared(mine, qq);
-#pragma unroll
-        for (int e = 0; e < kEpiSets; ++e) {
-          float v;
-          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(rem + (e * NB + m) * BM * 4) : "memory");
-          acc += v;
-        }
-      }
-      if (m < p.M && n < p.N) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc * p.gscale);
-    }
-  }
-  if (splits > 1) cluster_sync();         // remote partials stay alive until read
-  __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp) {                 // every tcgen05 access of the CTA has completed
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  const bool failed = *abort_flag != 0;
+  if (failed) {
+    // Every copy has landed before the CTA may exit. Without an abort the
+    // consumers waited for each one already.
+    if (warp == kTmaWarp && lane == 0)
+      for (int t = max(0, raw_issued - SR); t < raw_issued; ++t)
+        mbar_wait(bar(bars, B::kRawFull + t % SR), (t / SR) & 1, p.err);
+    if (warp == kActWarp && lane == 0)
+      for (int j = max(0, act_issued - SB); j < act_issued; ++j)
+        mbar_wait(bar(bars, B::kBLoad + j % SB), (j / SB) & 1, p.err);
+  }
+  const int rpr = (BM + splits - 1) / splits;
+  float* recv = reinterpret_cast<float*>(smem + L::kRecvOff);
+  const int et = threadIdx.x - kEpiWarp0 * 32;   // epilogue thread 0..255
+  constexpr int kEpiThreads = 4 * kEpiSets * 32;
+  if (et >= 0 && et < kEpiThreads) {
+    for (int i = et; i < NB * BM; i += kEpiThreads) {
+      const int m = i / BM, r = i - m * BM;
+      float s = red[m * BM + r];
+#pragma unroll
+      for (int e = 1; e < kEpiSets; ++e) s += red[(e * NB + m) * BM + r];
+      const int owner = r / rpr;
+      const uint32_t dst = smem_u32(recv + (rank * NB + m) * rpr + (r - owner * rpr));
+      st_dsmem_f32(splits > 1 ? mapa_shared(dst, owner) : dst, s);
+    }
+  }
+  if (splits > 1) cluster_sync();         // pushes visible to their owners
+  else __syncthreads();
+  if (et >= 0 && et < kEpiThreads && !failed) {
+    for (int i = et; i < NB * rpr; i += kEpiThreads) {
+      const int m = i / rpr, lr = i - m * rpr;
+      const int r = rank * rpr + lr;
+      if (m >= p.M || r >= BM || F::raw_row(r) >= F::kRows || (F::kQ2 && (r & 31) == 31)) continue;
+      const int n = n0 + F::raw_row(r);
+      if (n >= p.N) continue;
+      float acc = recv[m * rpr + lr];
+      for (int q = 1; q < splits; ++q) acc += recv[(q * NB + m) * rpr + lr];
+      p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(acc * p.gscale);
+    }
   }
 }
 
@@ -693,8 +718,9 @@ cudaError_t launch_tc_nb(const CUtensorMap& mw, const CUtensorMap& mw2, const CU
 template <class F>
 cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, const CUtensorMap& mw2, cudaStream_t s) {
   CUtensorMap ma;
+  const int nb = a.M <= 1 ? 1 : (a.M <= 2 ? 2 : (a.M <= 4 ? 4 : (a.M <= 8 ? 8 : 16)));   // box rows = NB
   cudaError_t e = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, static_cast<uint64_t>(a.K),
-                              static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda) * 2, 64, BN,
+                              static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda) * 2, 64, nb,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   const int tiles = (a.N + F::kRows - 1) / F::kRows;
