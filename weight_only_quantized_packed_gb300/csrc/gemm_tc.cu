@@ -54,17 +54,16 @@
 //   25..26 MMA (alternate groups; 25 allocates TMEM): per group one wait,
 //          then the elected lane issues the 8 MMAs into the group's
 //          accumulator slot and commits once ("MMA of group j done");
-//   27..28 activation operand hand-off (alternate groups): Q2_0 tiles are
-//          prepared in place on the tile the TMA loaded; FP8 tiles are used
-//          as loaded;
+//   27..28 Q2_0 activation operand hand-off: tiles are prepared in place
+//          on the tile the TMA loaded (FP8 and W4 tiles are used as loaded);
 //   29     TMA of the activation tiles (lane 0).
-// The MMA warp waits on a single barrier per group, "group j may start",
-// which completes after nine arrivals: the four converter warps of the set,
-// the activation operand (its hand-off warp) and
-// the four epilogue warps releasing the accumulator slot (pre-armed for the
-// first NACC groups). Every mbarrier wait costs a warp about 150 cycles of
-// latency even when the phase has completed, so a role keeps several groups
-// in flight by spreading them over several warps.
+// The MMA warp waits on one barrier per group, "group j may start", which
+// completes after the four converter warps of the set, the four epilogue
+// warps releasing the accumulator slot (pre-armed for the first NACC groups)
+// and, for Q2_0, the operand hand-off warp; for FP8 and W4 it then waits for
+// the activation tile's copy itself. A warp wakes about 120 cycles after the
+// arrival that completes a phase, so a role keeps several groups in flight
+// by spreading them over several warps.
 // Q2_0 tiles are 124 weight rows: the last lane of each 32-lane quarter of
 // TMEM (lanes 31, 63, 95, 127) holds a row of all-ones codes, whose
 // accumulator is 2^-69 * sum_k a_k, the group sum the fold needs, computed by
@@ -101,7 +100,11 @@ constexpr uint32_t kTmemCols = 512;
 static_assert(kAccCol + NACC * 16 <= kTmemCols, "TMEM budget");
 constexpr int SB = 16;             // activation operand stages (a CTA of <= 16 groups loads them all at once)
 constexpr int ND = 16;             // "MMA of group j done" and "group j may start" rings
-constexpr int kGoCount = 4 + 1 + 4;   // converter warps + operand + epilogue warps
+// "Group j may start": the converter warps, the epilogue warps releasing the
+// accumulator slot and, for Q2_0, the operand hand-off warp. FP8 and W4 tiles
+// are used as loaded: the MMA warp waits for the tile's copy itself.
+template <class F>
+__host__ __device__ constexpr int go_count() { return 4 + 4 + (F::kQ2 ? 1 : 0); }
 constexpr int NSC = 16;            // per-group row-scale ring (converters -> epilogue)
 
 // Ring depth: a scale slot of group j is rewritten after the MMA of group
@@ -161,8 +164,7 @@ struct Fp8Tc {
   __device__ static int raw_row(int r) { return r; }
   // Row r of the stage's group -> 64 TMEM columns from tcol: chunk c (K 16c..16c+15)
   // is MMA step c, natural pairs (16c + 2i, 16c + 2i + 1) in columns 8c + i.
-  template <int GI>
-  __device__ static void convert(const uint8_t* raw, int r, uint32_t tcol, float& d) {
+  __device__ static void convert(const uint8_t* raw, int r, int /*gi*/, uint32_t tcol, float& d) {
     const uint8_t* row = raw + r * 128;
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
@@ -200,28 +202,38 @@ struct Q2Tc {
                                    uint32_t bar, uint64_t pol) {
     tma_load_2d_hint(dst, m, g0 * 17, n0, bar, pol);              // 17 u16 per block
   }
-  // Block GI of row r: its 34 bytes start OFF = 34 GI mod 16 bytes into a
-  // 48-byte window of three aligned 16-byte chunks. Word i of the block
-  // (codes 16i..16i+15) is MMA step i: columns 8i + j (j < 4) hold the pair
-  // (c_j, c_{j+8}) of the word, columns 8i + 4 + j the pair (c_{j+4}, c_{j+12}),
-  // both scaled by 4^j. The last lane of each quarter writes codes 1
-  // everywhere (it reads the quarter's first row and discards it).
-  template <int GI>
-  __device__ static void convert(const uint8_t* raw, int r, uint32_t tcol, float& d) {
-    constexpr int b0 = 34 * GI;
-    constexpr int base = b0 & ~15;
-    constexpr int off = b0 - base;                 // 0, 2, ..., 14
+  // Block gi of row r: its 34 bytes start off = 34 gi mod 16 bytes into a
+  // 48-byte window of three aligned 16-byte chunks (one code path for every
+  // gi: the window's words are realigned with selects and a funnel shift).
+  // Word i of the block (codes 16i..16i+15) is MMA step i: columns 8i + j
+  // (j < 4) hold the pair (c_j, c_{j+8}) of the word, columns 8i + 4 + j the
+  // pair (c_{j+4}, c_{j+12}), both scaled by 4^j. The last lane of each
+  // quarter writes codes 1 everywhere (it reads the quarter's first row and
+  // discards it).
+  __device__ static void convert(const uint8_t* raw, int r, int gi, uint32_t tcol, float& d) {
+    const int b0 = 34 * gi;
+    const int base = b0 & ~15;
+    const int off = b0 - base;                     // 0, 2, ..., 14
+    const int k0 = off >> 2;                       // first window word of the block
+    const uint32_t sh = static_cast<uint32_t>(off & 3) * 8;   // 0 or 16
     const bool ones = (r & 31) == 31;
     const uint8_t* row = raw + raw_row(ones ? (r & ~31) : r) * 272 + base;
     const uint4 c0 = lds128(row), c1 = lds128(row + 16), c2 = lds128(row + 32);
     const uint32_t wv[12] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w, c2.x, c2.y, c2.z, c2.w};
+    uint32_t a[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const uint32_t lo = (k0 & 1) ? wv[i + 1] : wv[i];
+      const uint32_t hi = (k0 & 1) ? wv[i + 3] : wv[i + 2];
+      a[i] = (k0 & 2) ? hi : lo;
+    }
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       uint32_t v[16];
 #pragma unroll
       for (int w2 = 0; w2 < 2; ++w2) {
-        const int idx = off / 4 + 2 * h + w2;
-        uint32_t q = (off % 4 == 0) ? wv[idx] : __funnelshift_r(wv[idx], wv[idx + 1], 16);
+        const int idx = 2 * h + w2;
+        uint32_t q = __funnelshift_r(a[idx], a[idx + 1], sh);
         q = ones ? 0x55555555u : q;
         const uint32_t q8 = q >> 8;
 #pragma unroll
@@ -232,8 +244,7 @@ struct Q2Tc {
       }
       tmem_st16(tcol + 16 * h, v);
     }
-    constexpr int dw = (off + 32) / 4;
-    const uint32_t dbits = (off % 4 == 0) ? (wv[dw] & 0xFFFFu) : (wv[dw] >> 16);
+    const uint32_t dbits = (a[8] >> sh) & 0xFFFFu;
     d = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
   }
 };
@@ -258,16 +269,15 @@ struct W4Tc {
     tma_load_2d_hint(dst + kCodeBytes, m2, g0 * (GK / 16), n0, bar, pol); // scale bytes
   }
   __device__ static int raw_row(int r) { return r; }
-  // Row r, group GI of the stage -> 64 TMEM columns from tcol: 16-K step i is
+  // Row r, group gi of the stage -> 64 TMEM columns from tcol: 16-K step i is
   // code bytes 8i..8i+7 of the group and scale byte i; natural pairs
   // (16i + 2b, 16i + 2b + 1) = byte b in column 8i + b.
-  template <int GI>
-  __device__ static void convert(const uint8_t* raw, int r, uint32_t tcol, float& d) {
+  __device__ static void convert(const uint8_t* raw, int r, int gi, uint32_t tcol, float& d) {
     const uint8_t* row = raw + r * 128;
-    const uint2 sc = *reinterpret_cast<const uint2*>(raw + kCodeBytes + r * 16 + GI * 8);
+    const uint2 sc = *reinterpret_cast<const uint2*>(raw + kCodeBytes + r * 16 + gi * 8);
 #pragma unroll
     for (int h = 0; h < 4; ++h) {                              // one code chunk = steps 2h, 2h+1
-      const int c = 4 * GI + h;
+      const int c = 4 * gi + h;
       const uint4 x = lds128(row + ((c ^ (r & 7)) << 4));
       const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
       uint32_t v[16];
@@ -313,20 +323,20 @@ struct Bar {
   static constexpr int kRawFull = 0;                  // [SR]  raw stage landed
   static constexpr int kRawEmpty = kRawFull + F::kSR; // [SR]  raw stage converted
   static constexpr int kBLoad = kRawEmpty + F::kSR;   // [SB]  activation tile landed (Q2_0)
-  static constexpr int kGo = kBLoad + SB;             // [ND]  group j may start (kGoCount)
+  static constexpr int kGo = kBLoad + SB;             // [ND]  group j may start (go_count)
   static constexpr int kDone = kGo + ND;              // [ND]  MMA of group j complete
   static constexpr int kSclFull = kDone + ND;         // [NSC] row scales written
   static constexpr int kCount = kSclFull + NSC;
 };
 __device__ __forceinline__ uint32_t bar(uint32_t base, int i) { return base + 8u * static_cast<uint32_t>(i); }
 
-// Convert group GI of raw stage t for this thread's row. False on abort.
-template <class F, int GI>
-__device__ __forceinline__ bool convert_group(const uint8_t* raw, int t, int q, int r, int lane,
+// Convert group gi of raw stage t for this thread's row. False on abort.
+template <class F>
+__device__ __forceinline__ bool convert_group(const uint8_t* raw, int t, int gi, int q, int r, int lane,
                                               uint32_t tmem, uint32_t bars, float* scl, unsigned* err,
                                               volatile int* abort_flag) {
   using B = Bar<F>;
-  const int j = t * F::kGPR + GI;
+  const int j = t * F::kGPR + gi;
   const int so = j % SO;
   if (j >= SO) {
     const int g = j - SO;                            // previous user of the stage
@@ -335,12 +345,11 @@ __device__ __forceinline__ bool convert_group(const uint8_t* raw, int t, int q, 
   }
   tc_fence_after();
   float d;
-  F::template convert<GI>(raw, r, tmem + (static_cast<uint32_t>(q * 32) << 16) + so * 64, d);
+  F::convert(raw, r, gi, tmem + (static_cast<uint32_t>(q * 32) << 16) + so * 64, d);
   tmem_wait_st();
   if (F::kQ2) scl[(j % NSC) * BM + r] = d;
   tc_fence_before();
-  __threadfence_block();
-  __syncwarp();
+  __syncwarp();                                      // the arrive below releases the whole warp's work
   if (lane == 0) {
     mbar_arrive(bar(bars, B::kGo + j % ND));
     if (F::kQ2) mbar_arrive(bar(bars, B::kSclFull + j % NSC));
@@ -382,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t count = 1;
       // Converter warps that release a raw stage: the sets owning its groups.
       if (i >= B::kRawEmpty && i < B::kBLoad) count = 4 * (GPR < kConvSets ? GPR : kConvSets);
-      if (i >= B::kGo && i < B::kDone) count = kGoCount;
+      if (i >= B::kGo && i < B::kDone) count = go_count<F>();
       if (i >= B::kSclFull) count = 4;
       mbar_init(bar(bars, i), count);
     }
@@ -464,7 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j0 = (warp - kMmaWarp) * kMmaBatch; j0 < ng; j0 += kMmaWarps * kMmaBatch) {
       const int j1 = min(j0 + kMmaBatch, ng);
       bool ok = true;
-      for (int j = j0; j < j1 && ok; ++j) ok = wait_or_abort(bar(bars, B::kGo + j % ND), (j / ND) & 1, p.err, abort_flag);
+      for (int j = j0; j < j1 && ok; ++j) {
+        ok = wait_or_abort(bar(bars, B::kGo + j % ND), (j / ND) & 1, p.err, abort_flag);
+        if (!F::kQ2 && ok) ok = wait_or_abort(bar(bars, B::kBLoad + j % SB), (j / SB) & 1, p.err, abort_flag);
+      }
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
       if (elect_one()) {
@@ -504,23 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = wait_or_abort(bar(bars, B::kRawFull + sr), (t / SR) & 1, p.err, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       const uint8_t* raw = smem + L::kRawOff + sr * F::kRawBytes;
-      bool live;
-#define WQP_CONV(GI) convert_group<F, GI>(raw, t, q, r, lane, tmem, bars, scl, p.err, abort_flag)
       static_assert(GPR == 1 || GPR == 2 || GPR == 2 * kConvSets, "groups of a raw stage per converter set");
+      bool live;
       if constexpr (GPR == 1) {
-        live = WQP_CONV(0);
+        live = convert_group<F>(raw, t, 0, q, r, lane, tmem, bars, scl, p.err, abort_flag);
       } else if constexpr (GPR == 2) {
-        live = (h & 1) ? WQP_CONV(1) : WQP_CONV(0);
-      } else if (h == 0) {
-        live = WQP_CONV(0) && WQP_CONV(4);
-      } else if (h == 1) {
-        live = WQP_CONV(1) && WQP_CONV(5);
-      } else if (h == 2) {
-        live = WQP_CONV(2) && WQP_CONV(6);
+        live = convert_group<F>(raw, t, h & 1, q, r, lane, tmem, bars, scl, p.err, abort_flag);
       } else {
-        live = WQP_CONV(3) && WQP_CONV(7);
+        live = convert_group<F>(raw, t, h, q, r, lane, tmem, bars, scl, p.err, abort_flag) &&
+               convert_group<F>(raw, t, h + kConvSets, q, r, lane, tmem, bars, scl, p.err, abort_flag);
       }
-#undef WQP_CONV
       if (!live) break;
       if (lane == 0) mbar_arrive(bar(bars, B::kRawEmpty + sr));
     }
@@ -570,25 +575,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < NB; ++m) red[(es * NB + m) * BM + r] = acc[m];
     }
-  } else if (warp >= kPrepWarp0 && warp < kPrepWarp0 + kPrepWarps) {
+  } else if (F::kQ2 && warp >= kPrepWarp0 && warp < kPrepWarp0 + kPrepWarps) {
     // ------------------------------------------------------------ operand hand-off
-    // Warp p prepares groups j = p mod 2. Thread (row m, half) rewrites MMA
-    // steps 4 half .. 4 half + 3 in place: the natural chunks
-    // k = 16i..16i+7 and 16i+8..16i+15 of row m become the pairs
-    // (16i + c', 16i + c' + 8), c' = 0..7, times 2^(64 - 2 (c' mod 4)).
+    // Q2_0 activation tiles are rewritten in place before the MMA reads them:
+    // in row m, the natural chunks k = 16i..16i+7 and 16i+8..16i+15 become
+    // the pairs (16i + c', 16i + c' + 8), c' = 0..7, times 2^(64 - 2 (c' mod 4)).
+    // One item = (row m, box half, chunk pair st) = two 16-byte chunks; a
+    // warp spreads the items of kTPB tiles over its lanes (rows m >= M are
+    // zero-filled and skipped), makes the writes visible to the tensor core
+    // once per pass and then releases the tiles. Warp p takes the passes
+    // p mod 2.
+    constexpr int kItems = NB * 8;                        // items per tile
+    constexpr int kTPB = kItems >= 32 ? 1 : 32 / kItems;  // tiles per pass
+    constexpr int kSub = kItems > 32 ? kItems / 32 : 1;   // sub-passes per tile
     const int pw = warp - kPrepWarp0;
-    const int m = lane >> 1;
-    const int half = lane & 1;
-    const bool act = m < p.M;
+    const int tb = kItems >= 32 ? 0 : lane / kItems;      // this lane's tile in the pass
     constexpr uint32_t kS0 = 0x5F805F80u, kS1 = 0x5E805E80u, kS2 = 0x5D805D80u, kS3 = 0x5C805C80u;
-    for (int j = pw; j < ng; j += kPrepWarps) {
+    for (int jb = pw * kTPB; jb < ng; jb += kPrepWarps * kTPB) {
+      const int j = jb + tb;
+      const bool mine = j < ng;
       const int sb = j % SB;
-      const bool got = wait_or_abort(bar(bars, B::kBLoad + sb), (j / SB) & 1, p.err, abort_flag);
+      const bool got = !mine || wait_or_abort(bar(bars, B::kBLoad + sb), (j / SB) & 1, p.err, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
-      if (F::kQ2 && act) {
-        uint8_t* rowp = smem + L::kBOff + sb * kBBytes + half * (kBBytes / 2) + m * 128;
 #pragma unroll
-        for (int st = 0; st < 4; ++st) {
+      for (int sp = 0; sp < kSub; ++sp) {
+        const int it = kItems >= 32 ? sp * 32 + lane : lane % kItems;
+        const int m = it >> 3, half = (it >> 2) & 1, st = it & 3;
+        if (mine && m < p.M) {
+          uint8_t* rowp = smem + L::kBOff + sb * kBBytes + half * (kBBytes / 2) + m * 128;
           uint8_t* p0 = rowp + (((2 * st) ^ (m & 7)) << 4);
           uint8_t* p1 = rowp + (((2 * st + 1) ^ (m & 7)) << 4);
           const uint4 x = lds128(p0);
@@ -607,9 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       fence_proxy_async_smem();
-      __threadfence_block();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(bars, B::kGo + j % ND));
+      if (lane < kTPB && jb + lane < ng) mbar_arrive(bar(bars, B::kGo + (jb + lane) % ND));
     }
   }
 
