@@ -72,6 +72,8 @@
 // the partial sums are added in rank order through distributed shared memory
 // (deterministic, no global scratch). A kernel that allocates tensor memory
 // runs one CTA per SM, so a CTA takes all 512 TMEM columns and deep rings.
+#include <atomic>
+
 #include "decode.cuh"
 #include "tc.cuh"
 
@@ -81,31 +83,39 @@ namespace tc {
 constexpr int BM = 128;            // TMEM lanes = MMA M
 constexpr int BN = 16;             // activation rows (MMA N)
 constexpr int GK = 128;            // K per group = scale granularity
-constexpr int kConvSets = 4;       // converter warps 0..15
-constexpr int kEpiWarp0 = 16;      // epilogue warps 16..23, two sets
-constexpr int kEpiSets = 2;
-constexpr int kTmaWarp = 24;
-constexpr int kMmaWarp = 25;       // MMA warps 25..26; 25 allocates TMEM
-constexpr int kMmaWarps = 2;
+// Two CTAs share an SM (each 16 warps x 64 registers, 256 TMEM columns and
+// under half the shared memory), so one CTA's latency chain overlaps
+// another's: the split-K ranks of a small call, or the next call's CTAs,
+// which start loading and converting their weights under programmatic
+// dependent launch while this call finishes.
+constexpr int kCtasPerSm = 2;
+constexpr int kConvSets = 2;       // converter warps 0..7
+constexpr int kEpiWarp0 = 8;       // epilogue warps 8..11
+constexpr int kEpiSets = 1;
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;       // MMA warp; allocates TMEM
+constexpr int kMmaWarps = 1;
 constexpr int kMmaBatch = 1;       // groups issued per wait of the MMA warp
-constexpr int kPrepWarp0 = 27;     // activation hand-off warps 27..28
-constexpr int kPrepWarps = 2;
-constexpr int kActWarp = 29;       // activation TMA (its own warp: divergent lanes of one warp
+constexpr int kPrepWarp0 = 14;     // Q2_0 activation hand-off warp
+constexpr int kPrepWarps = 1;
+constexpr int kActWarp = 15;       // activation TMA (its own warp: divergent lanes of one warp
                                    // that wait on different barriers delay each other)
-constexpr int kThreads = 30 * 32;
-constexpr int SO = 6;              // TMEM operand stages, one group (64 columns) each
-constexpr int NACC = 8;            // TMEM accumulator slots, 16 columns each
+constexpr int kThreads = 16 * 32;
+constexpr int SO = 3;              // TMEM operand stages, one group (64 columns) each
+constexpr int NACC = 4;            // TMEM accumulator slots, 16 columns each
 constexpr uint32_t kAccCol = SO * 64;
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 256;
 static_assert(kAccCol + NACC * 16 <= kTmemCols, "TMEM budget");
-constexpr int SB = 16;             // activation operand stages (a CTA of <= 16 groups loads them all at once)
+static_assert(kCtasPerSm * kTmemCols <= 512, "TMEM columns of the co-resident CTAs");
+static_assert(kCtasPerSm * kThreads * 64 <= 65536, "registers of the co-resident CTAs at 64 per thread");
+constexpr int SB = 6;              // activation operand stages
 constexpr int ND = 16;             // "MMA of group j done" and "group j may start" rings
 // "Group j may start": the converter warps, the epilogue warps releasing the
 // accumulator slot and, for Q2_0, the operand hand-off warp. FP8 and W4 tiles
 // are used as loaded: the MMA warp waits for the tile's copy itself.
 template <class F>
 __host__ __device__ constexpr int go_count() { return 4 + 4 + (F::kQ2 ? 1 : 0); }
-constexpr int NSC = 16;            // per-group row-scale ring (converters -> epilogue)
+constexpr int NSC = 8;             // per-group row-scale ring (converters -> epilogue)
 
 // Ring depth: a scale slot of group j is rewritten after the MMA of group
 // j - SO completed; that MMA was issued after the epilogue released group
@@ -151,7 +161,7 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 struct Fp8Tc {
   static constexpr int kRows = 128;              // weight rows per tile
   static constexpr int kGPR = 1;
-  static constexpr int kSR = 8;
+  static constexpr int kSR = 4;
   static constexpr int kRawBytes = BM * GK;      // stage stride
   static constexpr int kBoxBytes = kRows * GK;   // bytes one stage load delivers
   static constexpr bool kQ2 = false;
@@ -190,7 +200,7 @@ struct Fp8Tc {
 struct Q2Tc {
   static constexpr int kRows = 124;              // + an all-ones row per lane quarter
   static constexpr int kGPR = 8;
-  static constexpr int kSR = 3;
+  static constexpr int kSR = 2;
   static constexpr int kRawBytes = BM * 8 * 34;  // stage stride
   // TMEM lane r = 32 q + l holds weight row 31 q + l for l < 31; lane 31 of
   // each quarter is the all-ones row.
@@ -256,7 +266,7 @@ struct Q2Tc {
 struct W4Tc {
   static constexpr int kRows = 128;
   static constexpr int kGPR = 2;
-  static constexpr int kSR = 8;
+  static constexpr int kSR = 4;
   static constexpr int kCodeBytes = BM * 128;
   static constexpr int kRawBytes = kCodeBytes + BM * 16;   // stage stride (1024-multiple)
   static constexpr int kBoxBytes = kRawBytes;
@@ -313,7 +323,9 @@ struct Layout {
   static constexpr int kBytes = kRecvOff + kRecvBytes;
   static constexpr int kAlloc = kBytes + 1024;                     // slack for 1024-byte alignment
   static_assert(kEpiSets * BM * BN * 4 <= F::kSR * F::kRawBytes, "split-K partials alias the raw ring");
-  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+  // Per SM: 228 KB of shared memory, 1 KB of it reserved per CTA, plus the
+  // kernel's static shared memory (< 1 KB).
+  static_assert(kCtasPerSm * (kAlloc + 2048) <= 228 * 1024, "shared memory budget of the co-resident CTAs");
 };
 
 // All mbarriers of a CTA live in one shared array; Bar<F>::X is the index of
@@ -358,7 +370,7 @@ __device__ __forceinline__ bool convert_group(const uint8_t* raw, int t, int gi,
 }
 
 template <class F, int NB>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
               const __grid_constant__ CUtensorMap tmA, TcParams p) {
   using L = Layout<F>;
@@ -503,29 +515,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ convert
     const int q = warp & 3;                 // TMEM lane quarter = 32-row block
-    const int h = warp >> 2;                // converter set: groups j = h mod 4
+    const int h = warp >> 2;                // converter set
     const int r = q * 32 + lane;
     float* scl = reinterpret_cast<float*>(smem + L::kSclOff);
-    // Set h converts the groups j = h mod 4: with one group per raw stage the
-    // stages t = h mod 4, with two the group h % 2 of stages t = h / 2 mod 2,
-    // with eight the groups h and h + 4 of every stage.
-    const int t0 = GPR == 1 ? h : (GPR == 2 ? (h >> 1) : 0);
-    const int dt = GPR == 1 ? kConvSets : (GPR == 2 ? 2 : 1);
+    // Set h converts, in every raw stage it takes, the groups gi = h mod
+    // kConvSets when a stage holds at least kConvSets groups; otherwise the
+    // group h mod GPR of every (kConvSets / GPR)-th stage.
+    constexpr int kGPS = GPR >= kConvSets ? GPR / kConvSets : 1;   // groups per set and stage
+    static_assert(GPR % kConvSets == 0 || kConvSets % GPR == 0, "groups of a raw stage per converter set");
+    const int t0 = GPR >= kConvSets ? 0 : h / GPR;
+    const int dt = GPR >= kConvSets ? 1 : kConvSets / GPR;
+    const int g0 = GPR >= kConvSets ? h : h % GPR;
     for (int t = t0; t < nst; t += dt) {
       const int sr = t % SR;
       const bool got = wait_or_abort(bar(bars, B::kRawFull + sr), (t / SR) & 1, p.err, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       const uint8_t* raw = smem + L::kRawOff + sr * F::kRawBytes;
-      static_assert(GPR == 1 || GPR == 2 || GPR == 2 * kConvSets, "groups of a raw stage per converter set");
-      bool live;
-      if constexpr (GPR == 1) {
-        live = convert_group<F>(raw, t, 0, q, r, lane, tmem, bars, scl, p.err, abort_flag);
-      } else if constexpr (GPR == 2) {
-        live = convert_group<F>(raw, t, h & 1, q, r, lane, tmem, bars, scl, p.err, abort_flag);
-      } else {
-        live = convert_group<F>(raw, t, h, q, r, lane, tmem, bars, scl, p.err, abort_flag) &&
-               convert_group<F>(raw, t, h + kConvSets, q, r, lane, tmem, bars, scl, p.err, abort_flag);
-      }
+      bool live = true;
+      for (int k = 0; k < kGPS && live; ++k)
+        live = convert_group<F>(raw, t, g0 + k * kConvSets, q, r, lane, tmem, bars, scl, p.err, abort_flag);
       if (!live) break;
       if (lane == 0) mbar_arrive(bar(bars, B::kRawEmpty + sr));
     }
@@ -680,15 +688,65 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-// CTAs per tile: one wave of one CTA per SM (a kernel that allocates tensor
-// memory runs one CTA per SM), at most 8 (portable cluster size) and at most
-// one raw stage per CTA.
+// Same block size, registers and shared memory as tc_kernel<F, *>, without
+// tensor-memory instructions: the occupancy calculator reports one CTA per SM
+// for any kernel that allocates tensor memory, while two such CTAs of 256
+// columns do run side by side, so cluster capacities are taken from this twin.
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) tc_capacity_twin() {}
+
+constexpr int kMaxDevices = 64;
+
+// Clusters of s CTAs (1 <= s <= 8) of format F that are resident at once on
+// the current device (0 if the query failed). Cached per device.
+template <class F>
+int cluster_capacity(int s) {
+  static std::atomic<int> cache[kMaxDevices][9];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int v = cache[dev][s].load(std::memory_order_relaxed);
+  if (v != 0) return v > 0 ? v : 0;
+  using L = Layout<F>;
+  int n = 0;
+  cudaError_t e = cudaFuncSetAttribute(tc_capacity_twin, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_capacity_twin, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  if (e == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = s;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&n, tc_capacity_twin, &cfg);
+  }
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();              // the query's failure is not the caller's error
+    n = 0;
+  }
+  cache[dev][s].store(n > 0 ? n : -1, std::memory_order_relaxed);
+  return n;
+}
+
+// CTAs per tile (the cluster's K split): the largest s <= 8 (portable
+// cluster size), at most one raw stage per CTA, for which all tiles' clusters
+// are resident at once; clusters live inside one GPC, so the capacity is
+// queried, not derived from the SM count (which only serves when the query
+// fails).
+template <class F>
 int choose_splits(int tiles, int stages, int num_sms) {
-  int s = num_sms / tiles;
-  if (s < 1) s = 1;
-  if (s > 8) s = 8;
-  if (s > stages) s = stages;
-  return s;
+  int best = 1;
+  for (int sp = 2; sp <= 8 && sp <= stages; ++sp) {
+    const int cap = cluster_capacity<F>(sp);
+    const bool fits = cap > 0 ? tiles <= cap : sp * tiles <= kCtasPerSm * num_sms;
+    if (fits) best = sp;
+  }
+  return best;
 }
 
 template <class F, int NB>
@@ -746,7 +804,7 @@ cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, const CUtensorMa
   p.K = a.K;
   p.ldc = a.ldc;
   p.stages = a.K / (GK * F::kGPR);
-  p.splits = choose_splits(tiles, p.stages, a.num_sms);
+  p.splits = choose_splits<F>(tiles, p.stages, a.num_sms);
   p.err = a.err;
   if (a.M <= 1) return launch_tc_nb<F, 1>(mw, mw2, ma, p, tiles, a.pdl, s);
   if (a.M <= 2) return launch_tc_nb<F, 2>(mw, mw2, ma, p, tiles, a.pdl, s);
