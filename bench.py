@@ -37,8 +37,8 @@ sys.path.insert(0, ROOT)
 METRIC = "effective weight-stream GB/s (% of GB300 HBM peak) and us/call at M=1..16"
 UNIT = "GB/s"
 # The step calls, for each M, the library's faster Q2_0 path at this shape
-# (measured): the scalar GEMV at M = 1, the tensor-core GEMM at M = 4 and 8.
-HEADLINE = {"fmt": "q2", "N": 5120, "K": 5120, "Ms": (1, 4, 8), "tc": {1: False, 4: True, 8: True}}
+# (measured): the tensor-core GEMM at M = 1, 4 and 8.
+HEADLINE = {"fmt": "q2", "N": 5120, "K": 5120, "Ms": (1, 4, 8), "tc": {1: True, 4: True, 8: True}}
 KERNEL_SOURCES = {False: ["gemv_scalar.cuh", "gemv_q2.cu", "decode.cuh", "common.cuh"],
                   True: ["gemm_tc.cu", "tc.cuh", "decode.cuh", "common.cuh"]}
 
@@ -286,7 +286,7 @@ def sweep(l2, peak):
             w.free()
             torch.cuda.empty_cache()
         # Decoder-layer sequence: qkv, o, gate+up, down, 8 layers cycled;
-        # scalar at M = 1, tensor core above.
+        # tensor core at every M (the faster path on each of these shapes).
         layer = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
         ws = [Workload("q2", N, K, (1, 4, 8, 16), 0, 4, cap_bytes=0) for (N, K) in layer]
         for w in ws:
@@ -294,9 +294,9 @@ def sweep(l2, peak):
             w.W = [w.W[0]] + [w.W[0].clone() for _ in range(7)]
         lb = sum(w.wb for w in ws)
         for M in (1, 4, 8, 16):
-            us = time_calls(lambda: [w.call(M, tc=M > 1) for w in ws], 40)
+            us = time_calls(lambda: [w.call(M, tc=True) for w in ws], 40)
             out.append({"workload": "q2 decoder layer (qkv+o+gate_up+down), 8 layers cycled", "M": M,
-                        "path": "q2_gemv" if M == 1 else "q2_gemm_tc",
+                        "path": "q2_gemm_tc",
                         "us_per_layer": round(us, 3), "gbs": round(lb / us / 1e3, 1),
                         "pct_peak": round(100 * lb / us / 1e3 / peak, 1)})
         del ws

@@ -42,36 +42,34 @@
 // on its own weight row and activation row.
 //
 // One CTA = one tile of weight rows x a contiguous range of 128-K groups (a
-// multiple of the raw stage). Warps:
-//   0..15  converters, in four sets (set = warp / 4 takes groups j = set
-//          mod 4), TMEM lane quarter = warp % 4; each thread converts one
-//          weight row of one group (64 columns);
-//   16..23 epilogue, two sets of four (alternate groups): per group,
-//          tcgen05.ld of the group's accumulator slot (lane = weight row,
-//          column = activation row) and the FP32 fold; each set keeps its own
-//          partial sums, added in a fixed order at the end;
-//   24     TMA of the raw weight stages (lane 0);
-//   25..26 MMA (alternate groups; 25 allocates TMEM): per group one wait,
-//          then the elected lane issues the 8 MMAs into the group's
-//          accumulator slot and commits once ("MMA of group j done");
-//   27..28 Q2_0 activation operand hand-off: tiles are prepared in place
-//          on the tile the TMA loaded (FP8 and W4 tiles are used as loaded);
-//   29     TMA of the activation tiles (lane 0).
+// multiple of the raw stage). Two CTAs share an SM (16 warps, 256 TMEM
+// columns and under half the shared memory each). Warps:
+//   0..7   converters, in two sets (set h takes the groups h mod 2 of a raw
+//          stage, or every other stage when a stage holds one group); TMEM
+//          lane quarter = warp % 4; each thread converts one weight row of
+//          one group (64 columns) into one of SO operand slots;
+//   8..11  epilogue: per group, tcgen05.ld of the group's accumulator slot
+//          (lane = weight row, column = activation row) and the FP32 fold;
+//   12     TMA of the raw weight stages (lane 0);
+//   13     MMA (allocates TMEM): per group one wait, then the elected lane
+//          issues the 8 MMAs into the group's accumulator slot and commits
+//          once ("MMA of group j done");
+//   14..15 Q2_0: activation operand, read from global memory and written
+//          permuted and pre-scaled into the MMA's activation slot;
+//   15     FP8, W4: TMA of the activation tiles (lane 0), used as loaded.
 // The MMA warp waits on one barrier per group, "group j may start", which
 // completes after the four converter warps of the set, the four epilogue
 // warps releasing the accumulator slot (pre-armed for the first NACC groups)
-// and, for Q2_0, the operand hand-off warp; for FP8 and W4 it then waits for
-// the activation tile's copy itself. A warp wakes about 120 cycles after the
-// arrival that completes a phase, so a role keeps several groups in flight
-// by spreading them over several warps.
+// and, for Q2_0, the operand warp; for FP8 and W4 it then waits for the
+// activation tile's copy itself.
 // Q2_0 tiles are 124 weight rows: the last lane of each 32-lane quarter of
 // TMEM (lanes 31, 63, 95, 127) holds a row of all-ones codes, whose
 // accumulator is 2^-69 * sum_k a_k, the group sum the fold needs, computed by
 // the same MMAs and read by each epilogue warp from its own lane 31.
 // When N is small, K is split over a thread-block cluster of up to 8 CTAs;
-// the partial sums are added in rank order through distributed shared memory
-// (deterministic, no global scratch). A kernel that allocates tensor memory
-// runs one CTA per SM, so a CTA takes all 512 TMEM columns and deep rings.
+// each rank owns a slice of the tile's rows, the others push their partial
+// sums into its shared memory, and it adds them in rank order
+// (deterministic, no global scratch).
 #include <atomic>
 
 #include "decode.cuh"
@@ -96,10 +94,10 @@ constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;       // MMA warp; allocates TMEM
 constexpr int kMmaWarps = 1;
 constexpr int kMmaBatch = 1;       // groups issued per wait of the MMA warp
-constexpr int kPrepWarp0 = 14;     // Q2_0 activation hand-off warp
-constexpr int kPrepWarps = 1;
-constexpr int kActWarp = 15;       // activation TMA (its own warp: divergent lanes of one warp
-                                   // that wait on different barriers delay each other)
+constexpr int kPrepWarp0 = 14;     // Q2_0: activation operand warps 14..15
+constexpr int kPrepWarps = 2;
+constexpr int kActWarp = 15;       // FP8, W4: activation TMA (its own warp: divergent lanes of
+                                   // one warp that wait on different barriers delay each other)
 constexpr int kThreads = 16 * 32;
 constexpr int SO = 3;              // TMEM operand stages, one group (64 columns) each
 constexpr int NACC = 4;            // TMEM accumulator slots, 16 columns each
@@ -139,6 +137,8 @@ constexpr int kBBytes = BN * GK * 2;
 constexpr int kRecvBytes = BN * (BM + 8) * 4;
 
 struct TcParams {
+  const uint16_t* A;       // bf16 [M, lda] (Q2_0 operand warps read it directly)
+  int lda;
   const float* scales;     // FP8: [ceil(N/128), K/128]; Q2_0, W4: unused here
   float gscale;            // W4 per-tensor scale (1 otherwise)
   uint16_t* C;
@@ -418,7 +418,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   pdl_launch_dependents();
 
   int raw_issued = 0, act_issued = 0;     // copies issued by lane 0 of the TMA / activation warp
-  if (warp == kTmaWarp || warp == kActWarp) {
+  // Producer warps: the raw-weight TMA and, for FP8 and W4, the activation TMA.
+  constexpr int kProducers = F::kQ2 ? 1 : 2;
+  const bool producer = warp == kTmaWarp || (!F::kQ2 && warp == kActWarp);
+  if (producer) {
     // ------------------------------------------------------------ TMA
     // Lane 0 of the TMA warp streams raw weight stages (independent of the
     // previous grid, so they start before griddepcontrol.wait); lane 0 of the
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                      bar(bars, B::kRawFull + sr), pol);
         raw_issued = t + 1;
       }
-    } else if (warp == kActWarp && lane == 0) {
+    } else if (!F::kQ2 && warp == kActWarp && lane == 0) {
       // Activation tiles [NB rows x 128 K] (rows >= M zero-filled) into the
       // operand ring; Q2_0 tiles are rewritten in place by the preparation
       // warps before the MMA reads them.
@@ -463,10 +466,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       tmem_relinquish();
       tc_fence_before();
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 64) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32 * kProducers) : "memory");
     tc_fence_after();
   }
-  const uint32_t tmem = (warp == kTmaWarp || warp == kActWarp) ? 0u : tmem_base_sh;
+  const uint32_t tmem = producer ? 0u : tmem_base_sh;
   // Partial sums [kEpiSets][NB][BM] for the final reduction alias the raw
   // ring: an epilogue set writes them only after the MMAs of the last two
   // groups (one per MMA warp) completed, so every raw stage has been consumed
@@ -584,49 +587,72 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int m = 0; m < NB; ++m) red[(es * NB + m) * BM + r] = acc[m];
     }
   } else if (F::kQ2 && warp >= kPrepWarp0 && warp < kPrepWarp0 + kPrepWarps) {
-    // ------------------------------------------------------------ operand hand-off
-    // Q2_0 activation tiles are rewritten in place before the MMA reads them:
-    // in row m, the natural chunks k = 16i..16i+7 and 16i+8..16i+15 become
-    // the pairs (16i + c', 16i + c' + 8), c' = 0..7, times 2^(64 - 2 (c' mod 4)).
-    // One item = (row m, box half, chunk pair st) = two 16-byte chunks; a
-    // warp spreads the items of kTPB tiles over its lanes (rows m >= M are
-    // zero-filled and skipped), makes the writes visible to the tensor core
-    // once per pass and then releases the tiles. Warp p takes the passes
-    // p mod 2.
+    // ------------------------------------------------------------ Q2_0 activation operand
+    // The operand is written straight from global memory into the MMA's
+    // activation slot: in row m, the natural chunks k = 16i..16i+7 and
+    // 16i+8..16i+15 become the pairs (16i + c', 16i + c' + 8), c' = 0..7,
+    // times 2^(64 - 2 (c' mod 4)). One item = (row m, box half, step pair st)
+    // = 32 contiguous bytes of A; a warp spreads the items of kTPB tiles over
+    // its lanes (rows m >= M are skipped: they only reach accumulator columns
+    // nothing reads), loads the next unit while it transforms this one, makes
+    // a pass's writes visible to the tensor core once and releases its tiles.
+    // Warp w takes the passes w mod 2.
     constexpr int kItems = NB * 8;                        // items per tile
     constexpr int kTPB = kItems >= 32 ? 1 : 32 / kItems;  // tiles per pass
-    constexpr int kSub = kItems > 32 ? kItems / 32 : 1;   // sub-passes per tile
+    constexpr int kSub = kItems > 32 ? kItems / 32 : 1;   // units (32 items) per pass
     const int pw = warp - kPrepWarp0;
     const int tb = kItems >= 32 ? 0 : lane / kItems;      // this lane's tile in the pass
     constexpr uint32_t kS0 = 0x5F805F80u, kS1 = 0x5E805E80u, kS2 = 0x5D805D80u, kS3 = 0x5C805C80u;
-    for (int jb = pw * kTPB; jb < ng; jb += kPrepWarps * kTPB) {
-      const int j = jb + tb;
-      const bool mine = j < ng;
-      const int sb = j % SB;
-      const bool got = !mine || wait_or_abort(bar(bars, B::kBLoad + sb), (j / SB) & 1, p.err, abort_flag);
-      if (!__all_sync(0xFFFFFFFFu, got)) break;
+    pdl_wait();                                           // activations may come from the previous grid
+    // Unit u = (pass n, sub-pass sp); loads its 32 bytes into x, y.
+    auto load_unit = [&](int n, int sp, uint4& x, uint4& y) {
+      const int j = (pw + n * kPrepWarps) * kTPB + tb;
+      const int it = kItems >= 32 ? sp * 32 + lane : lane % kItems;
+      const int m = it >> 3;
+      if (j < ng && m < p.M) {
+        const uint16_t* src = p.A + static_cast<size_t>(m) * p.lda + static_cast<size_t>(g_begin + j) * GK +
+                              ((it >> 2) & 1) * 64 + (it & 3) * 16;
+        x = ld_nc_v4(src);
+        y = ld_nc_v4(src + 8);
+      }
+    };
+    uint4 cx = make_uint4(0, 0, 0, 0), cy = cx;
+    load_unit(0, 0, cx, cy);
+    bool live = true;
+    for (int n = 0; live; ++n) {
+      const int jb = (pw + n * kPrepWarps) * kTPB;
+      if (jb >= ng) break;
+      // The pass's slots are free once the MMAs of the tiles SB earlier completed.
+      bool ok = true;
+      if (lane < kTPB) {
+        const int g = jb + lane - SB;
+        if (g >= 0 && jb + lane < ng) ok = wait_or_abort(bar(bars, B::kDone + g % ND), (g / ND) & 1, p.err, abort_flag);
+      }
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
 #pragma unroll
       for (int sp = 0; sp < kSub; ++sp) {
+        uint4 nx = make_uint4(0, 0, 0, 0), ny = nx;
+        if (sp + 1 < kSub) load_unit(n, sp + 1, nx, ny);
+        else load_unit(n + 1, 0, nx, ny);
+        const int j = jb + tb;
         const int it = kItems >= 32 ? sp * 32 + lane : lane % kItems;
         const int m = it >> 3, half = (it >> 2) & 1, st = it & 3;
-        if (mine && m < p.M) {
-          uint8_t* rowp = smem + L::kBOff + sb * kBBytes + half * (kBBytes / 2) + m * 128;
-          uint8_t* p0 = rowp + (((2 * st) ^ (m & 7)) << 4);
-          uint8_t* p1 = rowp + (((2 * st + 1) ^ (m & 7)) << 4);
-          const uint4 x = lds128(p0);
-          const uint4 y = lds128(p1);
+        if (j < ng && m < p.M) {
+          uint8_t* rowp = smem + L::kBOff + (j % SB) * kBBytes + half * (kBBytes / 2) + m * 128;
           uint4 o0, o1;
-          o0.x = mul_bf16x2(__byte_perm(x.x, y.x, 0x5410), kS0);
-          o0.y = mul_bf16x2(__byte_perm(x.x, y.x, 0x7632), kS1);
-          o0.z = mul_bf16x2(__byte_perm(x.y, y.y, 0x5410), kS2);
-          o0.w = mul_bf16x2(__byte_perm(x.y, y.y, 0x7632), kS3);
-          o1.x = mul_bf16x2(__byte_perm(x.z, y.z, 0x5410), kS0);
-          o1.y = mul_bf16x2(__byte_perm(x.z, y.z, 0x7632), kS1);
-          o1.z = mul_bf16x2(__byte_perm(x.w, y.w, 0x5410), kS2);
-          o1.w = mul_bf16x2(__byte_perm(x.w, y.w, 0x7632), kS3);
-          *reinterpret_cast<uint4*>(p0) = o0;
-          *reinterpret_cast<uint4*>(p1) = o1;
+          o0.x = mul_bf16x2(__byte_perm(cx.x, cy.x, 0x5410), kS0);
+          o0.y = mul_bf16x2(__byte_perm(cx.x, cy.x, 0x7632), kS1);
+          o0.z = mul_bf16x2(__byte_perm(cx.y, cy.y, 0x5410), kS2);
+          o0.w = mul_bf16x2(__byte_perm(cx.y, cy.y, 0x7632), kS3);
+          o1.x = mul_bf16x2(__byte_perm(cx.z, cy.z, 0x5410), kS0);
+          o1.y = mul_bf16x2(__byte_perm(cx.z, cy.z, 0x7632), kS1);
+          o1.z = mul_bf16x2(__byte_perm(cx.w, cy.w, 0x5410), kS2);
+          o1.w = mul_bf16x2(__byte_perm(cx.w, cy.w, 0x7632), kS3);
+          *reinterpret_cast<uint4*>(rowp + (((2 * st) ^ (m & 7)) << 4)) = o0;
+          *reinterpret_cast<uint4*>(rowp + (((2 * st + 1) ^ (m & 7)) << 4)) = o1;
         }
+        cx = nx;
+        cy = ny;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -796,6 +822,8 @@ cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, const CUtensorMa
   if (e != cudaSuccess) return e;
   const int tiles = (a.N + F::kRows - 1) / F::kRows;
   TcParams p;
+  p.A = static_cast<const uint16_t*>(a.A);
+  p.lda = a.lda;
   p.scales = static_cast<const float*>(a.scales);
   p.gscale = a.gscale;
   p.C = static_cast<uint16_t*>(a.C);
