@@ -181,10 +181,13 @@ def test_full_size_parity(oracle_lib, fmt, N, K, Ms):
         assert_scalar_parity(C, ref, K, f"{fmt} full M={M} N={N} K={K}")
 
 
-def test_pdl_launch_same_result():
+@pytest.mark.parametrize("M", [1, 8])
+def test_pdl_launch_same_result(M):
+    """Back-to-back launches with programmatic dependent launch give the same
+    bits as a launch without it."""
     import weight_only_quantized_packed_gb300 as wqp
 
-    d = G.make("q2", 8, 640, 5120, seed=4)
+    d = G.make("q2", M, 640, 5120, seed=4)
     base = G.host_bits(G.run_gpu(d))
     wqp.set_pdl(True)
     try:
