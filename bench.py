@@ -484,9 +484,30 @@ def cpu_baseline(seconds=10.0, rows=None):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(wb * len(H["Ms"]) * n / dt / 1e9, 4), "unit": UNIT,
-            "cores": oracle.max_threads(), "kind": "oracle",
+    cores = oracle.max_threads()
+    line = {"value": round(wb * len(H["Ms"]) * n / dt / 1e9, 4), "unit": UNIT,
+            "cores": cores, "kind": "oracle",
             "sample": f"{n} x (q2 M=1,4,8 over {rows} of {N} rows, K={K}); {dt:.1f} s"}
+    # The same oracle on one host thread, on a sixteenth of the rows.
+    rows1 = max(8, rows // 16)
+    W1 = W[:rows1]
+    wb1 = synth.q2_weight_bytes(rows1, K)
+    oracle.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        n1 = 0
+        while True:
+            for M in H["Ms"]:
+                oracle.q2_gemv(As[M], W1, M, rows1, K)
+            n1 += 1
+            if time.perf_counter() - t0 >= seconds / 4:
+                break
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(cores)
+    line["one_thread"] = {"value": round(wb1 * len(H["Ms"]) * n1 / dt1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                          "sample": f"{n1} x (q2 M=1,4,8 over {rows1} of {N} rows, K={K}); {dt1:.1f} s"}
+    return line
 
 
 def reference_arm(args, rank, world):
