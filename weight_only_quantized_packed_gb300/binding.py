@@ -96,6 +96,12 @@ def _stream(stream):
     import torch
 
     if stream is None:
+        # The current stream's raw handle; torch.cuda.current_stream() builds
+        # a Python stream object, which costs about as much host time as a
+        # launch.
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return ctypes.c_void_p(raw(torch._C._cuda_getDevice()))
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
