@@ -198,6 +198,17 @@ int wqp_set_pdl(int enable);
  * WQP_ERR_CUDA. */
 int wqp_get_device_error(void);
 
+/* Self-test of the failure path (for tests): launches one small kernel that
+ * waits, through the same bounded mbarrier wait the GEMM kernels use, on a
+ * barrier nothing ever completes. After limit_us microseconds (1..10^6) of
+ * wall time the wait gives up, the kernel records the timeout in the device
+ * error word and returns, so the next wqp_get_device_error() reports
+ * WQP_ERR_DEVICE_TIMEOUT and the context stays usable. (The GEMM kernels'
+ * waits give up after 2 s.) No trap, fault or hang is involved. Returns
+ * WQP_ERR_INVALID_ARG for limit_us out of range, WQP_ERR_CUDA if the launch
+ * fails, else WQP_OK. */
+int wqp_selftest_wait_timeout(int limit_us, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* wqp_status_string(int status);
 

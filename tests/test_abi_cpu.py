@@ -75,6 +75,12 @@ def test_row_chunks_rejects_small_cap(L):
     assert L.wqp_row_chunks(0, 256, 5, 8, buf, 0) == 0
 
 
+def test_selftest_limit_is_validated_before_any_cuda_call(L):
+    for limit_us in (0, -3, 1000001):
+        assert L.wqp_selftest_wait_timeout(limit_us, None) == 1
+        assert b"limit_us" in L.wqp_last_error()
+
+
 def test_pdl_policy_roundtrip(L):
     old = L.wqp_set_pdl(1)
     assert L.wqp_set_pdl(old) == 1

@@ -14,7 +14,7 @@ import threading
 __all__ = [
     "WqpError", "lib", "lib_path", "q2_gemv", "q2_gemm_tc", "w4a16_gemv", "w4a16_gemm_tc", "w8a16_gemm", "w8a16_gemm_tc",
     "q2_dequant", "w4a16_dequant", "w8a16_dequant", "row_chunks", "set_pdl",
-    "get_device_error", "status_string", "EXPORTS", "MAX_M_PER_LAUNCH",
+    "get_device_error", "selftest_wait_timeout", "status_string", "EXPORTS", "MAX_M_PER_LAUNCH",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -45,6 +45,7 @@ EXPORTS = {
     "wqp_row_chunks": [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_longlong), _I],
     "wqp_set_pdl": [_I],
     "wqp_get_device_error": [],
+    "wqp_selftest_wait_timeout": [_I, _P],
     "wqp_status_string": [_I],
     "wqp_last_error": [],
     "wqp_abi_version": [],
@@ -241,3 +242,10 @@ def set_pdl(enable: bool) -> bool:
 def get_device_error() -> int:
     """Read and clear the device error word (synchronises the device)."""
     return lib().wqp_get_device_error()
+
+
+def selftest_wait_timeout(limit_us: int = 2000, stream=None) -> None:
+    """Launch the failure-path self-test: a kernel whose bounded wait on a
+    barrier nothing completes gives up after limit_us microseconds and records
+    the timeout in the device error word (read it with get_device_error())."""
+    _check(lib().wqp_selftest_wait_timeout(int(limit_us), _stream(stream)), "wqp_selftest_wait_timeout")

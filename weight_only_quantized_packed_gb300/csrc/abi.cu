@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "../../include/wqp.h"
+#include "common.cuh"
 #include "internal.h"
 
 using namespace wqp;
@@ -197,6 +198,23 @@ int run_dequant(int fmt, const void* W, const void* scales, float gscale, float*
 
 }  // namespace
 
+namespace wqp {
+// A bounded wait that nothing completes: one CTA waits, through the same
+// helper the GEMM kernels use, on an mbarrier no thread arrives on. The wait
+// gives up after limit_ns of wall time, records the timeout in the device
+// error word and the kernel returns (no trap, no fault, no hang).
+__global__ void wait_timeout_selftest_kernel(unsigned* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t never;
+  const uint32_t bar = smem_u32(&never);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_ns(bar, 0, err, limit_ns);
+}
+}  // namespace wqp
+
 extern "C" {
 
 int q2_gemv(const void* A, const void* W, const void* scales, void* C, int M, int N, int K,
@@ -287,6 +305,19 @@ int wqp_row_chunks(int M, int K, int N, int max_rows, long long* out, int cap) {
 }
 
 int wqp_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
+
+int wqp_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(WQP_ERR_INVALID_ARG, "wqp_selftest_wait_timeout: limit_us=%d outside 1..10^6", limit_us);
+  DeviceInfo* dev = nullptr;
+  int st = device_setup(&dev);
+  if (st != WQP_OK) return st;
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      dev->err, static_cast<uint64_t>(limit_us) * 1000u);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "wqp_selftest_wait_timeout");
+  return WQP_OK;
+}
 
 int wqp_get_device_error(void) {
   DeviceInfo* dev = nullptr;

@@ -51,16 +51,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after kSpinLimit polls (each try_wait itself blocks
-// for a hardware-defined interval), records WQP_DEV_ERR_TIMEOUT and returns
-// false. Callers then skip the rest of their work without touching smem that
-// a copy may still be writing.
-constexpr uint32_t kSpinLimit = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+// Bounded wait: gives up once kWaitLimitNs of wall time (the global
+// nanosecond timer) have passed without the phase completing, records
+// WQP_DEV_ERR_TIMEOUT and returns false. Callers then skip the rest of their
+// work without touching smem that a copy may still be writing. The limit is
+// in time, not polls: a CTA may legitimately wait as long as the previous
+// kernel on the stream runs (programmatic dependent launch starts it early).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// True once limit_ns have passed since t0; reads the timer every 64 calls.
+__device__ __forceinline__ bool wait_expired(uint32_t i, uint64_t t0, uint64_t limit_ns) {
+  return (i & 63u) == 63u && global_ns() - t0 > limit_ns;
+}
+__device__ __forceinline__ bool mbar_wait_ns(uint32_t bar, uint32_t parity, unsigned* err, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (wait_expired(i, t0, limit_ns)) break;
+  }
   set_error(err, WQP_DEV_ERR_TIMEOUT);
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+  return mbar_wait_ns(bar, parity, err, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------------ bulk copy

@@ -202,9 +202,12 @@ __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
 // CTA has already aborted (flag in shared memory).
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, unsigned* err,
                                               volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 255u && *abort_flag) return false;
+    if (wait_expired(i, t0, kWaitLimitNs)) break;
   }
   set_error(err, WQP_DEV_ERR_TIMEOUT);
   *abort_flag = 1;
