@@ -40,7 +40,10 @@ UNIT = "GB/s"
 # (measured): the tensor-core GEMM at M = 1, 4 and 8.
 HEADLINE = {"fmt": "q2", "N": 5120, "K": 5120, "Ms": (1, 4, 8), "tc": {1: True, 4: True, 8: True}}
 KERNEL_SOURCES = {False: ["gemv_scalar.cuh", "gemv_q2.cu", "decode.cuh", "common.cuh"],
-                  True: ["gemm_tc.cu", "tc.cuh", "decode.cuh", "common.cuh"]}
+                  True: ["gemm_tc.cu", "tc.cuh", "decode.cuh", "common.cuh"],
+                  "mma": ["gemm_mma.cu", "tc.cuh", "common.cuh"]}
+# Q2_0 entry point per path key (False: scalar, True: tcgen05, "mma": mma.sync).
+Q2_PATH = {False: "q2_gemv", True: "q2_gemm_tc", "mma": "q2_gemm_mma"}
 
 
 # ------------------------------------------------------------------ helpers
@@ -195,7 +198,9 @@ class Workload:
         A = self.A[M] if A is None else A
         C = self.C[M] if C is None else C
         tc = self.tc if tc is None else tc
-        if self.fmt == "q2" and tc:
+        if self.fmt == "q2" and tc == "mma":
+            wqp.q2_gemm_mma(A, self.W[j], self.N, self.K, out=C)
+        elif self.fmt == "q2" and tc:
             wqp.q2_gemm_tc(A, self.W[j], self.N, self.K, out=C)
         elif self.fmt == "q2":
             wqp.q2_gemv(A, self.W[j], self.N, self.K, out=C)
@@ -267,6 +272,7 @@ def sweep(l2, peak):
         ("q2_gemv N=256 K=512", "q2", 256, 512, (1,), False, 0),
         ("q2_gemv N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), False, 1),
         ("q2_gemm_tc N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), True, 1),
+        ("q2_gemm_mma N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), "mma", 1),
         ("w4a16_gemv N=5120 K=5120", "w4", 5120, 5120, tuple(range(1, 9)), False, 2),
         ("w4a16_gemm_tc N=5120 K=5120", "w4", 5120, 5120, (1, 4, 8, 16), True, 2),
         ("w8a16_gemm N=17408 K=5120", "w8", 17408, 5120, (1, 4, 8, 16), False, 3),
@@ -293,10 +299,10 @@ def sweep(l2, peak):
             w.nbuf = 8
             w.W = [w.W[0]] + [w.W[0].clone() for _ in range(7)]
         lb = sum(w.wb for w in ws)
-        for M in (1, 4, 8, 16):
-            us = time_calls(lambda: [w.call(M, tc=True) for w in ws], 40)
+        for path, M in [(p, M) for p in (True, "mma") for M in (1, 4, 8, 16)]:
+            us = time_calls(lambda: [w.call(M, tc=path) for w in ws], 40)
             out.append({"workload": "q2 decoder layer (qkv+o+gate_up+down), 8 layers cycled", "M": M,
-                        "path": "q2_gemm_tc",
+                        "path": Q2_PATH[path],
                         "us_per_layer": round(us, 3), "gbs": round(lb / us / 1e3, 1),
                         "pct_peak": round(100 * lb / us / 1e3 / peak, 1)})
         del ws
@@ -374,7 +380,7 @@ def gpu_arm(args, rank, world, local_rank):
     Mdom = max(avg, key=avg.get)
     us_dom = avg[Mdom]
     tc_dom = H["tc"][Mdom]
-    kname = "q2_gemm_tc" if tc_dom else "q2_gemv"
+    kname = Q2_PATH[tc_dom]
     achieved = w.wb / (us_dom * 1e-6) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
@@ -403,7 +409,7 @@ def gpu_arm(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; A ~ N(0,1) bf16, ternary codes U{0,1,2}, d U[0.01,0.05] fp16)",
         "config": {"workload": "Q2_0 GEMV N=5120 K=5120, one step = M=1, 4, 8 calls",
-                   "paths": {str(M): ("q2_gemm_tc" if H["tc"][M] else "q2_gemv") for M in H["Ms"]},
+                   "paths": {str(M): Q2_PATH[H["tc"][M]] for M in H["Ms"]},
                    "timing": f"CUDA graph of {G} steps replayed {args.steps // G} times",
                    "weight_bytes_per_call": w.wb, "weight_buffers_cycled": w.nbuf,
                    "l2": f"inputs larger than L2: {w.nbuf} weight buffers = {w.nbuf * w.wb / 2**20:.0f} MiB > 3x L2 ({l2 / 2**20:.0f} MiB)",
@@ -573,7 +579,7 @@ def profile_case(case, launches, pdl):
 
     parts = case.split(":")
     fmt, M, N, K = parts[0], int(parts[1]), int(parts[2]), int(parts[3])
-    tc = len(parts) > 4 and parts[4] == "tc"
+    tc = {"tc": True, "mma": "mma"}.get(parts[4], False) if len(parts) > 4 else False
     wqp.set_pdl(bool(pdl))
     # About 192 MiB of cycled weights: past L2 (129 MB), well under 1 GiB on the device.
     w = Workload(fmt, N, K, (M,), 64 << 20, 9, tc=tc, cap_bytes=1 << 30)
@@ -597,7 +603,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--case", default=None,
-                    help="profiling mode: run --launches calls of one shape, fmt:M:N:K[:tc] "
+                    help="profiling mode: run --launches calls of one shape, fmt:M:N:K[:tc|:mma] "
                          "(fmt q2|w4|w8), weights cycled past L2; prints one status line")
     ap.add_argument("--launches", type=int, default=6)
     args = ap.parse_args()

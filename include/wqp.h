@@ -91,6 +91,24 @@ int q2_gemm_tc(const void* A, const void* W, void* C, int M, int N, int K, void*
 int q2_gemm_tc_strided(const void* A, int lda, const void* W, void* C, int ldc,
                        int M, int N, int K, void* stream);
 
+/* Warp-level tensor-core form of q2_gemv (mma.sync m16n8k16, BF16 operands,
+ * FP32 accumulation), swap-AB with 16 weight rows by 8 activation rows per
+ * MMA. Each warp decodes its own code words straight into MMA operands in
+ * registers (the same exact encoding as q2_gemm_tc: c * 4^j * 2^-133 against
+ * a * 2^(64 - 2j)); each 128-K block's sum of (c - 1) * a is scaled by its
+ * inline d once, in FP32. The K range is split over the CTAs of a thread-block
+ * cluster and the partial sums are added in rank order in shared memory.
+ * Arguments, layouts and limits are those of q2_gemm_tc (1 <= M <= 16,
+ * K % 1024 == 0, |a| < 2^62); anything else gives WQP_ERR_INVALID_ARG.
+ * Numerics: the contract of w8a16_gemm_tc. Not bit-identical to q2_gemv or
+ * q2_gemm_tc. A row does not depend on the other rows of the call.
+ * Device-side waits are bounded as for the other kernels (see
+ * wqp_get_device_error).
+ */
+int q2_gemm_mma(const void* A, const void* W, void* C, int M, int N, int K, void* stream);
+int q2_gemm_mma_strided(const void* A, int lda, const void* W, void* C, int ldc,
+                        int M, int N, int K, void* stream);
+
 /* ---------------------------------------------------------------- W4A16 ---
  * 4-bit E2M1 weights with E4M3 group scales (NVFP4-style) decode GEMV.
  * The family is "spark_model/layers/w4a16_gemv_tiers.rs" (module docs: the

@@ -46,7 +46,9 @@ def make(fmt: str, M: int, N: int, K: int, seed: int):
 def run_gpu(d, tc: bool = False, A=None, out=None):
     A = d["dA"] if A is None else A
     N, K = d["N"], d["K"]
-    if d["fmt"] == "q2" and tc:
+    if d["fmt"] == "q2" and tc == "mma":
+        C = wqp.q2_gemm_mma(A, d["dW"], N, K, out=out)
+    elif d["fmt"] == "q2" and tc:
         C = wqp.q2_gemm_tc(A, d["dW"], N, K, out=out)
     elif d["fmt"] == "q2":
         C = wqp.q2_gemv(A, d["dW"], N, K, out=out)

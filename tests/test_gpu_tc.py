@@ -90,15 +90,22 @@ def test_tc_full_size(oracle_lib, N, K, Ms):
 
 
 # ------------------------------------------------------------------ Q2_0
+# Both tensor-core engines: tcgen05 through tensor memory (q2_gemm_tc) and the
+# warp-level mma.sync path (q2_gemm_mma).
+ENGINES = pytest.mark.parametrize("eng", [True, "mma"], ids=["tcgen05", "mma_sync"])
+
+
 @pytest.mark.parametrize("N,K", [(128, 1024), (200, 2048), (1000, 1024), (77, 3072), (384, 8192)])
-def test_q2_tc_parity_small(oracle_lib, N, K):
+@ENGINES
+def test_q2_tc_parity_small(oracle_lib, N, K, eng):
     for M in (1, 4, 16):
         d = G.make("q2", M, N, K, seed=500 + N + K + M)
-        C = G.host_bits(G.run_gpu(d, tc=True))
+        C = G.host_bits(G.run_gpu(d, tc=eng))
         _check_tc(oracle_lib, d, C, f"q2 M={M} N={N} K={K}")
 
 
-def test_q2_tc_exact_arithmetic_bit_exact(oracle_lib):
+@ENGINES
+def test_q2_tc_exact_arithmetic_bit_exact(oracle_lib, eng):
     """Codes -1/0/1 times small integers, power-of-two d: exact in any order."""
     r = np.random.default_rng(8)
     M, N, K = 16, 260, 3072
@@ -108,34 +115,37 @@ def test_q2_tc_exact_arithmetic_bit_exact(oracle_lib):
     dd = (2.0 ** -r.integers(2, 6, size=(N, K // 128))).astype(np.float16)
     W = synth.pack_q2(codes, dd)
     d = {"A": A, "dA": G.dev_bf16(A), "M": M, "N": N, "K": K, "fmt": "q2", "W": W, "dW": G.dev_u8(W)}
-    C = G.host_bits(G.run_gpu(d, tc=True))
+    C = G.host_bits(G.run_gpu(d, tc=eng))
     assert np.array_equal(C, G.run_oracle(oracle_lib, d).c)
 
 
-def test_q2_tc_rows_independent_and_k_rule():
+@ENGINES
+def test_q2_tc_rows_independent_and_k_rule(eng):
     import weight_only_quantized_packed_gb300 as wqp
 
     d = G.make("q2", 16, 5120, 5120, seed=21)
-    c16 = G.host_bits(G.run_gpu(d, tc=True))
+    c16 = G.host_bits(G.run_gpu(d, tc=eng))
     for m in (0, 7, 15):
-        one = G.host_bits(G.run_gpu(d, tc=True, A=d["dA"][m:m + 1]))
+        one = G.host_bits(G.run_gpu(d, tc=eng, A=d["dA"][m:m + 1]))
         assert np.array_equal(one[0], c16[m])
     bad = G.make("q2", 1, 64, 640, seed=2)
     with pytest.raises(wqp.WqpError):
-        G.run_gpu(bad, tc=True)          # K % 1024 != 0
+        G.run_gpu(bad, tc=eng)          # K % 1024 != 0
 
 
 @pytest.mark.parametrize("N,K,Ms", [(5120, 5120, (1, 4, 8, 16)), (7168, 5120, (8,)),
                                     (5120, 17408, (16,)), (34816, 5120, (4,))])
-def test_q2_tc_full_size(oracle_lib, N, K, Ms):
+@ENGINES
+def test_q2_tc_full_size(oracle_lib, N, K, Ms, eng):
     for M in Ms:
         d = G.make("q2", M, N, K, seed=synth.seed_for(1, M))
-        C = G.host_bits(G.run_gpu(d, tc=True))
+        C = G.host_bits(G.run_gpu(d, tc=eng))
         frac = _check_tc(oracle_lib, d, C, f"q2 full M={M} N={N} K={K}")
         assert frac > 0.99
 
 
-def test_q2_tc_activation_range(oracle_lib):
+@ENGINES
+def test_q2_tc_activation_range(oracle_lib, eng):
     """The pre-scale 2^(64 - 2j) stays exact for large and small activations
     (|a| up to 2^40 and down to 2^-40), within the stated range."""
     for scale in (2.0 ** 40, 2.0 ** -40):
@@ -143,7 +153,7 @@ def test_q2_tc_activation_range(oracle_lib):
         A = synth.activations(M, K, 77, scale=scale)
         W, _, _ = synth.q2_weights(N, K, 78)
         d = {"A": A, "dA": G.dev_bf16(A), "M": M, "N": N, "K": K, "fmt": "q2", "W": W, "dW": G.dev_u8(W)}
-        C = G.host_bits(G.run_gpu(d, tc=True))
+        C = G.host_bits(G.run_gpu(d, tc=eng))
         _check_tc(oracle_lib, d, C, f"q2 activation scale {scale:g}")
 
 

@@ -12,7 +12,7 @@ import os
 import threading
 
 __all__ = [
-    "WqpError", "lib", "lib_path", "q2_gemv", "q2_gemm_tc", "w4a16_gemv", "w4a16_gemm_tc", "w8a16_gemm", "w8a16_gemm_tc",
+    "WqpError", "lib", "lib_path", "q2_gemv", "q2_gemm_tc", "q2_gemm_mma", "w4a16_gemv", "w4a16_gemm_tc", "w8a16_gemm", "w8a16_gemm_tc",
     "q2_dequant", "w4a16_dequant", "w8a16_dequant", "row_chunks", "set_pdl",
     "get_device_error", "selftest_wait_timeout", "status_string", "EXPORTS", "MAX_M_PER_LAUNCH",
 ]
@@ -31,6 +31,8 @@ EXPORTS = {
     "q2_gemv_strided": [_P, _I, _P, _P, _I, _I, _I, _I, _P],
     "q2_gemm_tc": [_P, _P, _P, _I, _I, _I, _P],
     "q2_gemm_tc_strided": [_P, _I, _P, _P, _I, _I, _I, _I, _P],
+    "q2_gemm_mma": [_P, _P, _P, _I, _I, _I, _P],
+    "q2_gemm_mma_strided": [_P, _I, _P, _P, _I, _I, _I, _I, _P],
     "w4a16_gemv": [_P, _P, _P, _P, _I, _I, _I, _P],
     "w4a16_gemv_ex": [_P, _I, _P, _P, _F, _P, _I, _I, _I, _I, _P],
     "w4a16_gemm_tc": [_P, _P, _P, _P, _I, _I, _I, _P],
@@ -150,6 +152,16 @@ def q2_gemm_tc(A, W, N: int, K: int, out=None, stream=None):
     C = _out(A, M, N, out)
     _check(lib().q2_gemm_tc_strided(_ptr(A), lda, _ptr(W), _ptr(C), C.stride(0), M, N, K,
                                     _stream(stream)), "q2_gemm_tc")
+    return C
+
+
+def q2_gemm_mma(A, W, N: int, K: int, out=None, stream=None):
+    """Warp-level tensor-core (mma.sync swap-AB) form of q2_gemv, 1 <= M <= 16, K % 1024 == 0."""
+    _need_cuda(A, W, out)
+    M, lda = _rows(A, K)
+    C = _out(A, M, N, out)
+    _check(lib().q2_gemm_mma_strided(_ptr(A), lda, _ptr(W), _ptr(C), C.stride(0), M, N, K,
+                                     _stream(stream)), "q2_gemm_mma")
     return C
 
 

@@ -81,7 +81,7 @@ int device_setup(DeviceInfo** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-enum class Fmt { Q2, W4, W8, W8TC, Q2TC, W4TC };
+enum class Fmt { Q2, W4, W8, W8TC, Q2TC, W4TC, Q2MMA };
 
 const char* fmt_name(Fmt f) {
   switch (f) {
@@ -91,6 +91,7 @@ const char* fmt_name(Fmt f) {
     case Fmt::W8TC: return "w8a16_gemm_tc";
     case Fmt::Q2TC: return "q2_gemm_tc";
     case Fmt::W4TC: return "w4a16_gemm_tc";
+    case Fmt::Q2MMA: return "q2_gemm_mma";
   }
   return "?";
 }
@@ -99,16 +100,16 @@ int validate(Fmt f, const void* A, int lda, const void* W, const void* scales, v
              int M, int N, int K) {
   const char* nm = fmt_name(f);
   if (M < 0) return fail(WQP_ERR_INVALID_ARG, "%s: M=%d < 0", nm, M);
-  const bool tc = (f == Fmt::W8TC || f == Fmt::Q2TC || f == Fmt::W4TC);
+  const bool tc = (f == Fmt::W8TC || f == Fmt::Q2TC || f == Fmt::W4TC || f == Fmt::Q2MMA);
   const bool w4 = (f == Fmt::W4 || f == Fmt::W4TC);
-  const bool q2 = (f == Fmt::Q2 || f == Fmt::Q2TC);
+  const bool q2 = (f == Fmt::Q2 || f == Fmt::Q2TC || f == Fmt::Q2MMA);
   if (tc && (M < 1 || M > 16))
     return fail(WQP_ERR_INVALID_ARG, "%s: M=%d outside 1..16 (kernel M tile)", nm, M);
   if (N < 1 || N > (1 << 24)) return fail(WQP_ERR_INVALID_ARG, "%s: N=%d outside 1..2^24", nm, N);
   if (K < 128 || K > (1 << 20) || K % 128 != 0)
     return fail(WQP_ERR_INVALID_ARG, "%s: K=%d must be a multiple of 128 in [128, 2^20]", nm, K);
   if (!A || !W || !C) return fail(WQP_ERR_INVALID_ARG, "%s: NULL A, W or C", nm);
-  if (f == Fmt::Q2TC && K % 1024 != 0)
+  if ((f == Fmt::Q2TC || f == Fmt::Q2MMA) && K % 1024 != 0)
     return fail(WQP_ERR_INVALID_ARG, "%s: K=%d must be a multiple of 1024", nm, K);
   if (f == Fmt::W4TC && K % 256 != 0)
     return fail(WQP_ERR_INVALID_ARG, "%s: K=%d must be a multiple of 256", nm, K);
@@ -162,6 +163,7 @@ int run_gemm(Fmt f, const void* A, int lda, const void* W, const void* scales, f
       case Fmt::W8TC: e = launch_w8a16_gemm_tc(a, s); break;
       case Fmt::Q2TC: e = launch_q2_gemm_tc(a, s); break;
       case Fmt::W4TC: e = launch_w4a16_gemm_tc(a, s); break;
+      case Fmt::Q2MMA: e = launch_q2_gemm_mma(a, s); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, fmt_name(f));
   }
@@ -235,6 +237,15 @@ int q2_gemm_tc(const void* A, const void* W, void* C, int M, int N, int K, void*
 int q2_gemm_tc_strided(const void* A, int lda, const void* W, void* C, int ldc, int M, int N, int K,
                        void* stream) {
   return run_gemm(Fmt::Q2TC, A, lda, W, nullptr, 1.0f, C, ldc, M, N, K, stream);
+}
+
+int q2_gemm_mma(const void* A, const void* W, void* C, int M, int N, int K, void* stream) {
+  return run_gemm(Fmt::Q2MMA, A, K, W, nullptr, 1.0f, C, N, M, N, K, stream);
+}
+
+int q2_gemm_mma_strided(const void* A, int lda, const void* W, void* C, int ldc, int M, int N, int K,
+                        void* stream) {
+  return run_gemm(Fmt::Q2MMA, A, lda, W, nullptr, 1.0f, C, ldc, M, N, K, stream);
 }
 
 int w4a16_gemv(const void* A, const void* W, const void* scales, void* C, int M, int N, int K,

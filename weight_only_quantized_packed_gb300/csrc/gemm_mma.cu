@@ -1,0 +1,530 @@
+// Q2_0 GEMM for 1 <= M <= 16 on the warp-level tensor-core path
+// (mma.sync m16n8k16, BF16 operands, FP32 accumulation), swap-AB: the MMA's
+// 16 "rows" are weight rows n, its 8 "columns" are activation rows m.
+//
+// What it computes is the Q2_0 product of "Ternary Bonsai 8B on GB10: Q2_0
+// GEMV" (format and formula sections):
+//   C[m, n] = bf16( sum_k A[m, k] * (c[n, k] - 1) * d[n, k / 128] ),
+// the same result as q2_gemm_tc, to the tensor-core tolerance (the MMA sums
+// 16 products in its own order; see the "FP8 M=16 tensor-core" section of
+// "Bonsai ternary / FP8 decode kernels: M-dispatch, tiers and tensor cores").
+//
+// Why registers instead of tensor memory: the GEMV is a weight stream, and
+// every weight must pass through the converter exactly once. Feeding tcgen05
+// through tensor memory puts a store -> commit -> barrier -> MMA -> commit ->
+// barrier round trip on every 128-K group; here each warp turns its own code
+// words into MMA operands in registers and issues the MMAs itself, so nothing
+// waits on another warp except the stage hand-off.
+//
+// Layout of one CTA (BM = 64 weight rows x the CTA's K range):
+//   warps 0..7  compute: warp w owns rows 16 (w % 4) .. + 15 of the tile and
+//               blocks 4 (w / 4) .. + 3 of every stage (the two halves'
+//               partial sums are added in shared memory at the end);
+//   warp 8      producer: TMA of raw stages (64 rows x 8 blocks x 34 bytes).
+// Per 128-K block b and thread (g = lane / 4, t = lane % 4):
+//   * A fragment: code words 2t and 2t + 1 of the block, rows g and g + 8.
+//     Word bits 2q..2q+1 hold code q (q < 16). The pair of 16-bit lanes
+//     (code x, code 8 + x), masked in place by (word & 0x00030003 << 2x), is
+//     the BF16 pair (c_x 4^x, c_{8+x} 4^x) * 2^-133 (a subnormal or the
+//     smallest normal, exact); (word >> 8) gives codes (4 + x, 12 + x).
+//   * B fragment: activation rows m = g (and g + 8 for M > 8): the 32
+//     activations of k = 128 b + 32 t .. + 31, paired the same way and
+//     multiplied by 2^(64 - 2x), so every product is c * a * 2^-69 exactly.
+//   * The chain starts from -2^-69 * sum_k a (an MMA chain with every code 1
+//     and a negative sign, run once per block by the warp that prepares that
+//     block's B fragments), so it ends at 2^-69 * sum_k (c - 1) a.
+//   * acc += d * chain, and C = bf16(acc * 2^69).
+// Split-K: the CTAs of a cluster split the K stages. Rank 0 owns the tile:
+// every other rank sends its partial sums into rank 0's shared memory with
+// st.async (completing on an mbarrier of rank 0) and exits at once, freeing
+// its SM for the next grid; rank 0 adds them in rank order and stores.
+#include <atomic>
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace wqp {
+namespace mma {
+
+constexpr int BM = 64;                       // weight rows per CTA
+constexpr int kTiles = 4;                    // 16-row MMA tiles per CTA
+constexpr int kCompute = 2 * kTiles;         // compute warps: two per tile, four blocks each
+constexpr int kThreads = (kCompute + 1) * 32;
+constexpr int kBlocks = 8;                   // 128-K blocks per raw stage (1024 K)
+constexpr int kRowBytes = kBlocks * 34;      // 272: 17 x 16 bytes
+constexpr int kStageBytes = BM * kRowBytes;  // 17408
+constexpr int kFragBytes = 32 * 64;          // B fragments of one block, one 8-row m tile
+constexpr int kMaxSplits = 8;                // CTAs per cluster (K split) at most (portable size)
+
+// MT: m tiles of 8 activation rows, 1 (M <= 8) or 2 (M <= 16).
+// kMulti: a CTA runs more than one raw stage (two raw buffers, one refilled
+// while the other is consumed); otherwise exactly one.
+template <int MT, bool kMulti>
+struct Cfg {
+  static constexpr int SW = kMulti ? 2 : 1;                     // raw stage buffers
+  static constexpr int kBStage = kBlocks * MT * kFragBytes;      // B fragments of one stage
+  static constexpr int kSStage = kBlocks * MT * 32 * 8;          // -S fragments of one stage
+  static constexpr int kRawOff = 0;
+  static constexpr int kBOff = kRawOff + SW * kStageBytes;
+  static constexpr int kSOff = kBOff + kBStage;
+  // Partial sums of one set of four warps: 4 tiles x MT x 32 lanes x 4 floats.
+  static constexpr int kRecvSlot = kTiles * MT * 32 * 16;
+  static constexpr int kPairOff = kSOff + kSStage;               // second halves' sums, this CTA
+  static constexpr int kRecvOff = kPairOff + kRecvSlot;          // ranks 1.. of the cluster, at rank 0
+  // Dynamic shared memory for a cluster of `splits` CTAs.
+  static constexpr int bytes(int splits) { return kRecvOff + (splits - 1) * kRecvSlot; }
+  static_assert(kStageBytes % 1024 == 0 && kBOff % 16 == 0 && kSOff % 16 == 0 && kPairOff % 16 == 0 &&
+                    kRecvOff % 16 == 0, "align");
+  static_assert(2 * (bytes(kMaxSplits) + 1024) <= 227 * 1024, "shared memory per SM");
+};
+
+struct MmaParams {
+  const uint16_t* A;   // bf16 [M, lda]
+  uint16_t* C;         // bf16 [M, ldc]
+  int lda, ldc;
+  int M, N, K;
+  int stages;          // K / 1024
+  int splits;          // CTAs per tile = cluster size
+  unsigned* err;
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
+__device__ __forceinline__ void sts128(void* p, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Cluster barrier halves: the early arrive lets every rank know its peers
+// have started before anyone stores into their shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Four floats into a peer CTA's shared memory (shared::cluster address),
+// completing as 16 bytes on the peer's mbarrier.
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float x, float y, float z, float w, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(x), "f"(y), "f"(z), "f"(w), "r"(bar)
+               : "memory");
+}
+
+// Code words 2t and 2t + 1 of block b (compile time) of a raw row: 8 bytes
+// at 34 b + 8 t, 4-byte aligned for even b and 2 bytes off for odd b.
+template <int b>
+__device__ __forceinline__ void load_codes(const uint8_t* row, int t, uint32_t& w0, uint32_t& w1) {
+  if constexpr ((b & 1) == 0) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(row + 34 * b + 8 * t);
+    w0 = p[0];
+    w1 = p[1];
+  } else {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(row + 34 * b - 2 + 8 * t);
+    const uint32_t x0 = p[0], x1 = p[1], x2 = p[2];
+    w0 = __funnelshift_r(x0, x1, 16);
+    w1 = __funnelshift_r(x1, x2, 16);
+  }
+}
+template <int b>
+__device__ __forceinline__ float load_d(const uint8_t* row) {
+  return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(row + 34 * b + 32)));
+}
+
+// -(4^x) * 2^-133 in both BF16 lanes: the "code 1, negated" operand.
+__device__ __forceinline__ constexpr uint32_t neg_ones(int x) { return 0x80008000u | (0x00010001u << (2 * x)); }
+// 2^(64 - 2x) in both BF16 lanes.
+__device__ __forceinline__ constexpr uint32_t prescale(int x) { return ((191u - 2u * x) << 7) * 0x00010001u; }
+
+// kOcc: CTAs per SM the registers are budgeted for.
+template <int MT, bool kMulti, int kOcc>
+__global__ void __launch_bounds__(kThreads, kOcc)
+    q2_mma_kernel(const __grid_constant__ CUtensorMap tmW, const MmaParams p) {
+  using L = Cfg<MT, kMulti>;
+  constexpr int SW = L::SW;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[2 * SW + 1];   // full[SW], empty[SW], partial sums received
+  __shared__ int abort_sh;
+  volatile int* abort_flag = &abort_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int splits = p.splits;
+  const int tile = blockIdx.x / splits;
+  const int rank = blockIdx.x - tile * splits;   // == %cluster_ctarank
+  const int n0 = tile * BM;
+  const int st0 = (rank * p.stages) / splits;
+  const int T = kMulti ? ((rank + 1) * p.stages) / splits - st0 : 1;   // >= 1: splits <= stages
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[SW]), recv_bar = smem_u32(&bars[2 * SW]);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SW; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, kCompute);
+    }
+    mbar_init(recv_bar, 1);
+    mbar_fence_init();
+    if (rank == 0 && splits > 1) mbar_arrive_expect_tx(recv_bar, (splits - 1) * L::kRecvSlot);
+    abort_sh = 0;
+  }
+  if (splits > 1) cluster_arrive_relaxed();
+  __syncthreads();
+  pdl_launch_dependents();
+
+  float tot[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tot[mt][i] = 0.f;
+  const int g = lane >> 2, t4 = lane & 3;
+
+  if (warp == kCompute) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tmW);
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int s = t % SW;
+        if (t >= SW && !tc::wait_or_abort(empty0 + 8 * s, ((t / SW) - 1) & 1, p.err, abort_flag)) break;
+        mbar_arrive_expect_tx(full0 + 8 * s, kStageBytes);
+        tc::tma_load_2d_hint(smem_u32(smem + L::kRawOff + s * kStageBytes), &tmW, (st0 + t) * (kBlocks * 17),
+                             n0, full0 + 8 * s, pol);
+        issued = t + 1;
+      }
+      // The CTA may not exit with a copy into its shared memory in flight:
+      // stay until the last copies issued have landed.
+      for (int t = max(0, issued - SW); t < issued; ++t) mbar_wait(full0 + 8 * (t % SW), (t / SW) & 1, p.err);
+    }
+    __syncwarp();
+    if (splits > 1) cluster_wait();
+    return;
+  }
+
+  // -------------------------------------------------------------- compute
+  const int rt = warp % kTiles, half = warp / kTiles;
+  // Every rank has started (its barriers are initialised) before anyone
+  // sends to rank 0; waited here, where a CTA launched early waits anyway.
+  if (splits > 1) cluster_wait();
+  pdl_wait();                                     // activations (and C) may belong to the previous grid
+  const uint16_t* arow[MT];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const int m = min(g + 8 * mt, p.M - 1);       // rows past M: any valid row, results unused
+    arow[mt] = p.A + static_cast<size_t>(m) * p.lda + 32 * t4;
+  }
+  // Block `warp` of each stage is prepared by this warp.
+  uint4 act[MT][4];
+  auto load_act = [&](int t) {
+    const size_t k0 = static_cast<size_t>(kBlocks * (st0 + t) + warp) * 128;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) act[mt][q] = ld_nc_v4(arow[mt] + k0 + 8 * q);
+  };
+  // B fragments (permuted, pre-scaled) and the -S chain of the block.
+  auto store_b = [&]() {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const uint32_t r[16] = {act[mt][0].x, act[mt][0].y, act[mt][0].z, act[mt][0].w,
+                              act[mt][1].x, act[mt][1].y, act[mt][1].z, act[mt][1].w,
+                              act[mt][2].x, act[mt][2].y, act[mt][2].z, act[mt][2].w,
+                              act[mt][3].x, act[mt][3].y, act[mt][3].z, act[mt][3].w};
+      uint32_t bf[16];
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int x = s & 3, o = 8 * (s >> 2) + (x >> 1);
+        const uint32_t sel = (x & 1) ? 0x7632u : 0x5410u;
+        bf[2 * s] = mul_bf16x2(__byte_perm(r[o], r[o + 4], sel), prescale(x));
+        bf[2 * s + 1] = mul_bf16x2(__byte_perm(r[o + 2], r[o + 6], sel), prescale(x));
+      }
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t no = neg_ones(s & 3);
+        mma_bf16_16816(c, no, no, no, no, bf[2 * s], bf[2 * s + 1]);
+      }
+      uint8_t* dst = smem + L::kBOff + (warp * MT + mt) * kFragBytes + lane * 16;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        sts128(dst + q * 512, make_uint4(bf[4 * q], bf[4 * q + 1], bf[4 * q + 2], bf[4 * q + 3]));
+      reinterpret_cast<float2*>(smem + L::kSOff)[(warp * MT + mt) * 32 + lane] = make_float2(c[0], c[1]);
+    }
+  };
+
+  load_act(0);
+  bool live = true;
+  const int r0 = 16 * rt + g;
+  for (int t = 0; t < T; ++t) {
+    store_b();
+    asm volatile("bar.sync 1, %0;" ::"r"(kCompute * 32) : "memory");   // B of stage t complete
+    if (kMulti && t + 1 < T) load_act(t + 1);
+    const int s = t % SW;
+    if (live) live = tc::wait_or_abort(full0 + 8 * s, (t / SW) & 1, p.err, abort_flag);
+    live = __all_sync(0xFFFFFFFFu, live);
+    if (live) {
+      // This warp's four blocks start at block 4 half of the stage.
+      const uint8_t* rg = smem + L::kRawOff + s * kStageBytes + r0 * kRowBytes + 4 * 34 * half;
+      const uint8_t* rh = rg + 8 * kRowBytes;
+      const uint8_t* bs = smem + L::kBOff + 4 * half * MT * kFragBytes + lane * 16;
+      const float2* ss = reinterpret_cast<const float2*>(smem + L::kSOff) + 4 * half * MT * 32 + lane;
+      auto block = [&](auto jc) {
+        constexpr int j = decltype(jc)::value;   // block 4 half + j; 34 (4 half) keeps j's alignment
+        uint32_t wg0, wg1, wh0, wh1;
+        load_codes<j>(rg, t4, wg0, wg1);
+        load_codes<j>(rh, t4, wh0, wh1);
+        const float dg = load_d<j>(rg), dh = load_d<j>(rh);
+        const uint32_t wg[4] = {wg0, wg0 >> 8, wg1, wg1 >> 8};
+        const uint32_t wh[4] = {wh0, wh0 >> 8, wh1, wh1 >> 8};
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint8_t* bp = bs + (j * MT + mt) * kFragBytes;
+          const uint4 q0 = lds128(bp), q1 = lds128(bp + 512), q2 = lds128(bp + 1024), q3 = lds128(bp + 1536);
+          const uint32_t bf[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
+                                   q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+          const float2 ns = ss[(j * MT + mt) * 32];
+          float c[4] = {ns.x, ns.y, ns.x, ns.y};
+#pragma unroll
+          for (int st = 0; st < 8; ++st) {
+            const uint32_t m = 0x00030003u << (2 * (st & 3));
+            const int w = 2 * (st >> 2);
+            mma_bf16_16816(c, wg[w] & m, wh[w] & m, wg[w + 1] & m, wh[w + 1] & m, bf[2 * st], bf[2 * st + 1]);
+          }
+          tot[mt][0] = fmaf(dg, c[0], tot[mt][0]);
+          tot[mt][1] = fmaf(dg, c[1], tot[mt][1]);
+          tot[mt][2] = fmaf(dh, c[2], tot[mt][2]);
+          tot[mt][3] = fmaf(dh, c[3], tot[mt][3]);
+        }
+      };
+      block(std::integral_constant<int, 0>{});
+      block(std::integral_constant<int, 1>{});
+      block(std::integral_constant<int, 2>{});
+      block(std::integral_constant<int, 3>{});
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (kMulti && t + 1 < T)
+      asm volatile("bar.sync 1, %0;" ::"r"(kCompute * 32) : "memory");   // B buffer free for t + 1
+  }
+
+  // ------------------------------------------------------------ reduce + store
+  // The second half of each tile hands its partial sums to the first through
+  // shared memory (one named barrier per tile) and leaves; the first half
+  // adds them (first + second). Ranks 1.. then send their sums to rank 0,
+  // slot rank - 1 in this thread's fragment order, and leave; rank 0 adds
+  // the slots in rank order and stores.
+  float4* pair = reinterpret_cast<float4*>(smem + L::kPairOff) + rt * MT * 32 + lane;
+  if (half == 1) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) pair[mt * 32] = make_float4(tot[mt][0], tot[mt][1], tot[mt][2], tot[mt][3]);
+    asm volatile("bar.arrive %0, 64;" ::"r"(2 + rt) : "memory");
+    return;
+  }
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + rt) : "memory");
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const float4 v = pair[mt * 32];
+    tot[mt][0] += v.x;
+    tot[mt][1] += v.y;
+    tot[mt][2] += v.z;
+    tot[mt][3] += v.w;
+  }
+  if (rank != 0) {
+    const uint32_t dst = tc::mapa_shared(
+        smem_u32(smem + L::kRecvOff + (rank - 1) * L::kRecvSlot + (rt * MT * 32 + lane) * 16), 0);
+    const uint32_t bar0 = tc::mapa_shared(recv_bar, 0);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+      st_async_f4(dst + mt * 32 * 16, tot[mt][0], tot[mt][1], tot[mt][2], tot[mt][3], bar0);
+    return;
+  }
+  bool ok = splits == 1 || mbar_wait(recv_bar, 0, p.err);
+  ok = ok && live && *abort_flag == 0;
+  if (!ok) return;
+  const float kUnscale = __uint_as_float((127u + 69u) << 23);   // 2^69
+  const float4* recv = reinterpret_cast<const float4*>(smem + L::kRecvOff) + rt * MT * 32 + lane;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    float acc[4] = {tot[mt][0], tot[mt][1], tot[mt][2], tot[mt][3]};
+    for (int q = 1; q < splits; ++q) {            // rank order
+      const float4 v = recv[(q - 1) * (L::kRecvSlot / 16) + mt * 32];
+      acc[0] += v.x;
+      acc[1] += v.y;
+      acc[2] += v.z;
+      acc[3] += v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = r0 + 8 * (i >> 1);
+      const int m = 8 * mt + 2 * t4 + (i & 1);
+      if (m < p.M && n0 + r < p.N) p.C[static_cast<size_t>(m) * p.ldc + n0 + r] = f32_to_bf16_rn(acc[i] * kUnscale);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+constexpr int kMaxDevices = 64;
+
+// The compiled variants: (m tiles, several stages per CTA, CTAs per SM).
+// Single-stage M <= 8 calls have two register budgets: 3 CTAs per SM (63
+// registers) and 4 (56 registers) for grids that need the fourth slot.
+template <int MT, bool kMulti, int kOcc>
+struct Variant {
+  static constexpr auto kernel = q2_mma_kernel<MT, kMulti, kOcc>;
+};
+
+// Opt-in shared memory above 48 KB (up to the largest cluster's size) and the
+// whole carveout (several CTAs per SM). Set once, before the first launch or
+// occupancy query.
+template <int MT, bool kMulti, int kOcc>
+cudaError_t set_attrs() {
+  static std::atomic<int> done{0};
+  if (done.load(std::memory_order_acquire)) return cudaSuccess;
+  auto k = Variant<MT, kMulti, kOcc>::kernel;
+  cudaError_t e =
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MT, kMulti>::bytes(kMaxSplits));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  if (e == cudaSuccess) done.store(1, std::memory_order_release);
+  return e;
+}
+
+// CTAs of a variant resident at once in clusters of s (0 if the query
+// failed). Cached per device.
+template <int MT, bool kMulti, int kOcc>
+int resident_ctas(int s) {
+  static std::atomic<int> cache[kMaxDevices][kMaxSplits + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int v = cache[dev][s].load(std::memory_order_relaxed);
+  if (v != 0) return v > 0 ? v : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<MT, kMulti>::bytes(s);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = s;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (set_attrs<MT, kMulti, kOcc>() != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, Variant<MT, kMulti, kOcc>::kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();            // the query's failure is not the caller's error
+    n = 0;
+  }
+  cache[dev][s].store(n > 0 ? n * s : -1, std::memory_order_relaxed);
+  return n > 0 ? n * s : 0;
+}
+
+// K split per tile: minimise (waves of resident CTAs) x (stages per CTA);
+// ties go to the larger split (more copies in flight). Depends on N, K and
+// the device only, never on M, so a row's summation order does not depend on
+// the other rows of the call.
+int choose_splits(int tiles, int stages, int num_sms) {
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= kMaxSplits && s <= stages; ++s) {
+    const int per_cta = (stages + s - 1) / s;
+    int slots = per_cta > 1 ? resident_ctas<1, true, 3>(s) : resident_ctas<1, false, 4>(s);
+    if (slots <= 0) slots = 3 * num_sms;
+    const long long ctas = static_cast<long long>(tiles) * s;
+    const long long waves = (ctas + slots - 1) / slots;
+    const long long cost = waves * per_cta;
+    if (best_cost < 0 || cost <= best_cost) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+template <int MT, bool kMulti, int kOcc>
+cudaError_t launch_variant(const CUtensorMap& mw, const MmaParams& p, int tiles, bool pdl, cudaStream_t s) {
+  cudaError_t e = set_attrs<MT, kMulti, kOcc>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles * p.splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<MT, kMulti>::bytes(p.splits);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = p.splits;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, Variant<MT, kMulti, kOcc>::kernel, mw, p);
+}
+
+}  // namespace mma
+
+// Requires K % 1024 == 0 (checked by the caller): a row is then 34 * K / 128
+// bytes, a multiple of 16, and each raw stage of 8 blocks starts on a 16-byte
+// boundary (the TMA box's x = 136 * stage elements of 2 bytes).
+cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s) {
+  using namespace mma;
+  const uint64_t G = static_cast<uint64_t>(a.K / 128);
+  CUtensorMap mw;
+  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),
+                              34 * G, kBlocks * 17, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  MmaParams p;
+  p.A = static_cast<const uint16_t*>(a.A);
+  p.C = static_cast<uint16_t*>(a.C);
+  p.lda = a.lda;
+  p.ldc = a.ldc;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.stages = a.K / (kBlocks * 128);
+  p.splits = 1;
+  p.err = a.err;
+  const int tiles = (a.N + BM - 1) / BM;
+  p.splits = choose_splits(tiles, p.stages, a.num_sms);
+  const bool multi = (p.stages + p.splits - 1) / p.splits > 1;
+  if (a.M > 8)
+    return multi ? launch_variant<2, true, 2>(mw, p, tiles, a.pdl, s) : launch_variant<2, false, 2>(mw, p, tiles, a.pdl, s);
+  if (multi) return launch_variant<1, true, 3>(mw, p, tiles, a.pdl, s);
+  // Three CTAs per SM spread a grid that fits them over more SMs (the cluster
+  // scheduler fills an SM's free slots before the next SM's); four only when
+  // the grid needs the fourth slot to run in one wave.
+  const int ctas3 = resident_ctas<1, false, 3>(p.splits);
+  const bool fits3 = static_cast<long long>(tiles) * p.splits <= (ctas3 > 0 ? ctas3 : 3 * a.num_sms);
+  return fits3 ? launch_variant<1, false, 3>(mw, p, tiles, a.pdl, s) : launch_variant<1, false, 4>(mw, p, tiles, a.pdl, s);
+}
+
+}  // namespace wqp
