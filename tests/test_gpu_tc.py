@@ -157,6 +157,59 @@ def test_q2_tc_activation_range(oracle_lib, eng):
         _check_tc(oracle_lib, d, C, f"q2 activation scale {scale:g}")
 
 
+@ENGINES
+def test_q2_tc_strided_rows_and_canary(oracle_lib, eng):
+    """Row pitches lda > K and ldc > N, ragged N; bytes outside C's rows stay
+    untouched."""
+    import torch
+
+    M, N, K = 6, 200, 2048
+    d = G.make("q2", M, N, K, seed=19)
+    lda, ldc = K + 64, N + 13
+    Abig = torch.zeros((M, lda), dtype=torch.bfloat16, device="cuda")
+    Abig[:, :K] = d["dA"]
+    canary = torch.full((M + 2, ldc), -7.0, dtype=torch.bfloat16, device="cuda")
+    out = canary[1:M + 1].as_strided((M, N), (ldc, 1))
+    G.run_gpu(d, tc=eng, A=Abig[:, :K], out=out)
+    host = canary.float().cpu().numpy()
+    assert (host[0] == -7.0).all() and (host[M + 1] == -7.0).all()
+    assert (host[1:M + 1, N:] == -7.0).all()
+    C = G.host_bits(canary[1:M + 1, :N].contiguous())
+    _check_tc(oracle_lib, d, C, "q2 strided")
+
+
+@ENGINES
+def test_q2_tc_dependent_chain_under_pdl(eng):
+    """x_{i+1} = q2(x_i) with N = K: each call reads the previous call's
+    output and overwrites the buffer the call before it read. Launched with
+    programmatic dependent launch, the chain gives the same bits as without
+    it (the grid-dependency wait orders both)."""
+    import torch
+    import weight_only_quantized_packed_gb300 as wqp
+
+    M, N = 4, 5120
+    d = G.make("q2", M, N, N, seed=33)
+
+    f = wqp.q2_gemm_mma if eng == "mma" else wqp.q2_gemm_tc
+
+    def chain():
+        bufs = [d["dA"].clone(), torch.empty_like(d["dA"])]
+        for i in range(6):
+            f(bufs[i % 2], d["dW"], N, N, out=bufs[(i + 1) % 2])
+        torch.cuda.synchronize()
+        return G.host_bits(bufs[0])
+
+    base = chain()
+    wqp.set_pdl(True)
+    try:
+        runs = [chain() for _ in range(3)]
+    finally:
+        wqp.set_pdl(False)
+    for r in runs:
+        assert np.array_equal(r, base)
+    assert np.isfinite(bf16_to_f64(base)).all() and (base != 0).any()
+
+
 # ---------------------------------------------------------------- W4A16
 @pytest.mark.parametrize("N,K", [(128, 256), (200, 512), (1000, 1024), (77, 2560), (384, 4096)])
 def test_w4_tc_parity_small(oracle_lib, N, K):

@@ -55,7 +55,6 @@ constexpr int kThreads = (kCompute + 1) * 32;
 constexpr int kBlocks = 8;                   // 128-K blocks per raw stage (1024 K)
 constexpr int kRowBytes = kBlocks * 34;      // 272: 17 x 16 bytes
 constexpr int kStageBytes = BM * kRowBytes;  // 17408
-constexpr int kFragBytes = 32 * 64;          // B fragments of one block, one 8-row m tile
 constexpr int kMaxSplits = 8;                // CTAs per cluster (K split) at most (portable size)
 
 // MT: m tiles of 8 activation rows, 1 (M <= 8) or 2 (M <= 16).
@@ -63,20 +62,22 @@ constexpr int kMaxSplits = 8;                // CTAs per cluster (K split) at mo
 // while the other is consumed); otherwise exactly one.
 template <int MT, bool kMulti>
 struct Cfg {
-  static constexpr int SW = kMulti ? 2 : 1;                     // raw stage buffers
-  static constexpr int kBStage = kBlocks * MT * kFragBytes;      // B fragments of one stage
-  static constexpr int kSStage = kBlocks * MT * 32 * 8;          // -S fragments of one stage
+  static constexpr int SW = kMulti ? 2 : 1;                      // raw stage buffers
   static constexpr int kRawOff = 0;
-  static constexpr int kBOff = kRawOff + SW * kStageBytes;
-  static constexpr int kSOff = kBOff + kBStage;
-  // Partial sums of one set of four warps: 4 tiles x MT x 32 lanes x 4 floats.
-  static constexpr int kRecvSlot = kTiles * MT * 32 * 16;
-  static constexpr int kPairOff = kSOff + kSStage;               // second halves' sums, this CTA
-  static constexpr int kRecvOff = kPairOff + kRecvSlot;          // ranks 1.. of the cluster, at rank 0
+  // Every compute warp's partial sums (4 tiles x MT x 32 lanes x 4 floats),
+  // written over the raw buffers once all of them are consumed.
+  static constexpr int kSlot = kTiles * MT * 32 * 16;
+  static constexpr int kRedOff = 0;
+  static constexpr int kBody = SW * kStageBytes > kCompute * kSlot ? SW * kStageBytes : kCompute * kSlot;
+  // Multi-stage CTAs: the next stage's activations of each warp's block,
+  // copied ahead with cp.async ([warp][MT][4 chunks][32 lanes][16 bytes]).
+  static constexpr int kActOff = kBody;
+  static constexpr int kActWarp = MT * 4 * 32 * 16;
+  static constexpr int kActBytes = kMulti ? kCompute * kActWarp : 0;
+  static constexpr int kRecvOff = kActOff + kActBytes;            // ranks 1.. of the cluster, at rank 0
   // Dynamic shared memory for a cluster of `splits` CTAs.
-  static constexpr int bytes(int splits) { return kRecvOff + (splits - 1) * kRecvSlot; }
-  static_assert(kStageBytes % 1024 == 0 && kBOff % 16 == 0 && kSOff % 16 == 0 && kPairOff % 16 == 0 &&
-                    kRecvOff % 16 == 0, "align");
+  static constexpr int bytes(int splits) { return kRecvOff + (splits - 1) * kSlot; }
+  static_assert(kStageBytes % 1024 == 0 && kRecvOff % 16 == 0, "align");
   static_assert(2 * (bytes(kMaxSplits) + 1024) <= 227 * 1024, "shared memory per SM");
 };
 
@@ -105,18 +106,12 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-__device__ __forceinline__ uint4 lds128(const void* p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(smem_u32(p)));
-  return v;
+// 16-byte asynchronous global -> shared copy (L2 only), and its completion.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
-__device__ __forceinline__ void sts128(void* p, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Cluster barrier halves: the early arrive lets every rank know its peers
 // have started before anyone stores into their shared memory.
@@ -135,24 +130,28 @@ __device__ __forceinline__ void st_async_f4(uint32_t addr, float x, float y, flo
                : "memory");
 }
 
-// Code words 2t and 2t + 1 of block b (compile time) of a raw row: 8 bytes
-// at 34 b + 8 t, 4-byte aligned for even b and 2 bytes off for odd b.
-template <int b>
-__device__ __forceinline__ void load_codes(const uint8_t* row, int t, uint32_t& w0, uint32_t& w1) {
-  if constexpr ((b & 1) == 0) {
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(row + 34 * b + 8 * t);
+// Code words 2t and 2t + 1 of the block at `blk` (34 b bytes into a raw row):
+// 8 bytes at blk + 8 t. kA is the block's alignment class b % 4: 0 is
+// 8-byte aligned, 2 is 4-byte aligned, 1 and 3 are 2 bytes off.
+template <int kA>
+__device__ __forceinline__ void load_codes(const uint8_t* blk, int t, uint32_t& w0, uint32_t& w1) {
+  if constexpr (kA == 0) {
+    const uint2 v = *reinterpret_cast<const uint2*>(blk + 8 * t);
+    w0 = v.x;
+    w1 = v.y;
+  } else if constexpr (kA == 2) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(blk + 8 * t);
     w0 = p[0];
     w1 = p[1];
   } else {
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(row + 34 * b - 2 + 8 * t);
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(blk - 2 + 8 * t);
     const uint32_t x0 = p[0], x1 = p[1], x2 = p[2];
     w0 = __funnelshift_r(x0, x1, 16);
     w1 = __funnelshift_r(x1, x2, 16);
   }
 }
-template <int b>
-__device__ __forceinline__ float load_d(const uint8_t* row) {
-  return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(row + 34 * b + 32)));
+__device__ __forceinline__ float load_d(const uint8_t* blk) {
+  return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk + 32)));
 }
 
 // -(4^x) * 2^-133 in both BF16 lanes: the "code 1, negated" operand.
@@ -186,18 +185,13 @@ __global__ void __launch_bounds__(kThreads, kOcc)
     }
     mbar_init(recv_bar, 1);
     mbar_fence_init();
-    if (rank == 0 && splits > 1) mbar_arrive_expect_tx(recv_bar, (splits - 1) * L::kRecvSlot);
+    if (rank == 0 && splits > 1) mbar_arrive_expect_tx(recv_bar, (splits - 1) * L::kSlot);
     abort_sh = 0;
   }
   if (splits > 1) cluster_arrive_relaxed();
   __syncthreads();
   pdl_launch_dependents();
 
-  float tot[MT][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tot[mt][i] = 0.f;
   const int g = lane >> 2, t4 = lane & 3;
 
   if (warp == kCompute) {
@@ -224,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, kOcc)
   }
 
   // -------------------------------------------------------------- compute
-  const int rt = warp % kTiles, half = warp / kTiles;
+  // Warp w owns block w of every stage, for all 64 rows of the tile.
+  const int b = warp;
   // Every rank has started (its barriers are initialised) before anyone
   // sends to rank 0; waited here, where a CTA launched early waits anyway.
   if (splits > 1) cluster_wait();
@@ -235,152 +230,171 @@ __global__ void __launch_bounds__(kThreads, kOcc)
     const int m = min(g + 8 * mt, p.M - 1);       // rows past M: any valid row, results unused
     arow[mt] = p.A + static_cast<size_t>(m) * p.lda + 32 * t4;
   }
-  // Block `warp` of each stage is prepared by this warp.
+  // This thread's 32 activations of the block, per m tile: straight into
+  // registers for a single stage; for several, copied one stage ahead into
+  // this warp's shared buffer.
+  // Rows past M are never copied (no duplicate requests to the same lines):
+  // their lanes read the slot of row M - 1, which some lane copies.
   uint4 act[MT][4];
+  uint4* abuf = reinterpret_cast<uint4*>(smem + L::kActOff + warp * L::kActWarp);
+  auto act_src = [&](int t, int mt, int q) {
+    return arow[mt] + static_cast<size_t>(kBlocks * (st0 + t) + b) * 128 + 8 * q;
+  };
   auto load_act = [&](int t) {
-    const size_t k0 = static_cast<size_t>(kBlocks * (st0 + t) + warp) * 128;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) act[mt][q] = ld_nc_v4(arow[mt] + k0 + 8 * q);
-  };
-  // B fragments (permuted, pre-scaled) and the -S chain of the block.
-  auto store_b = [&]() {
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const uint32_t r[16] = {act[mt][0].x, act[mt][0].y, act[mt][0].z, act[mt][0].w,
-                              act[mt][1].x, act[mt][1].y, act[mt][1].z, act[mt][1].w,
-                              act[mt][2].x, act[mt][2].y, act[mt][2].z, act[mt][2].w,
-                              act[mt][3].x, act[mt][3].y, act[mt][3].z, act[mt][3].w};
-      uint32_t bf[16];
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const int x = s & 3, o = 8 * (s >> 2) + (x >> 1);
-        const uint32_t sel = (x & 1) ? 0x7632u : 0x5410u;
-        bf[2 * s] = mul_bf16x2(__byte_perm(r[o], r[o + 4], sel), prescale(x));
-        bf[2 * s + 1] = mul_bf16x2(__byte_perm(r[o + 2], r[o + 6], sel), prescale(x));
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (kMulti) {
+          if (g + 8 * mt < p.M) cp_async16(abuf + (mt * 4 + q) * 32 + lane, act_src(t, mt, q));
+        } else {
+          act[mt][q] = ld_nc_v4(act_src(t, mt, q));
+        }
       }
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t no = neg_ones(s & 3);
-        mma_bf16_16816(c, no, no, no, no, bf[2 * s], bf[2 * s + 1]);
-      }
-      uint8_t* dst = smem + L::kBOff + (warp * MT + mt) * kFragBytes + lane * 16;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        sts128(dst + q * 512, make_uint4(bf[4 * q], bf[4 * q + 1], bf[4 * q + 2], bf[4 * q + 3]));
-      reinterpret_cast<float2*>(smem + L::kSOff)[(warp * MT + mt) * 32 + lane] = make_float2(c[0], c[1]);
-    }
+    if constexpr (kMulti) cp_async_commit();
   };
+  float tot[kTiles][MT][4];
+#pragma unroll
+  for (int rt = 0; rt < kTiles; ++rt)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tot[rt][mt][i] = 0.f;
 
   load_act(0);
   bool live = true;
-  const int r0 = 16 * rt + g;
-  for (int t = 0; t < T; ++t) {
-    store_b();
-    asm volatile("bar.sync 1, %0;" ::"r"(kCompute * 32) : "memory");   // B of stage t complete
-    if (kMulti && t + 1 < T) load_act(t + 1);
-    const int s = t % SW;
-    if (live) live = tc::wait_or_abort(full0 + 8 * s, (t / SW) & 1, p.err, abort_flag);
-    live = __all_sync(0xFFFFFFFFu, live);
-    if (live) {
-      // This warp's four blocks start at block 4 half of the stage.
-      const uint8_t* rg = smem + L::kRawOff + s * kStageBytes + r0 * kRowBytes + 4 * 34 * half;
-      const uint8_t* rh = rg + 8 * kRowBytes;
-      const uint8_t* bs = smem + L::kBOff + 4 * half * MT * kFragBytes + lane * 16;
-      const float2* ss = reinterpret_cast<const float2*>(smem + L::kSOff) + 4 * half * MT * 32 + lane;
-      auto block = [&](auto jc) {
-        constexpr int j = decltype(jc)::value;   // block 4 half + j; 34 (4 half) keeps j's alignment
-        uint32_t wg0, wg1, wh0, wh1;
-        load_codes<j>(rg, t4, wg0, wg1);
-        load_codes<j>(rh, t4, wh0, wh1);
-        const float dg = load_d<j>(rg), dh = load_d<j>(rh);
-        const uint32_t wg[4] = {wg0, wg0 >> 8, wg1, wg1 >> 8};
-        const uint32_t wh[4] = {wh0, wh0 >> 8, wh1, wh1 >> 8};
+  auto run = [&](auto ac) {
+    constexpr int kA = decltype(ac)::value;
+    for (int t = 0; t < T; ++t) {
+      if constexpr (kMulti) {
+        cp_async_wait_all();                        // this thread's copies of stage t
+        __syncwarp();                               // and the other lanes' (rows past M)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const uint8_t* bp = bs + (j * MT + mt) * kFragBytes;
-          const uint4 q0 = lds128(bp), q1 = lds128(bp + 512), q2 = lds128(bp + 1024), q3 = lds128(bp + 1536);
-          const uint32_t bf[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
-                                   q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
-          const float2 ns = ss[(j * MT + mt) * 32];
-          float c[4] = {ns.x, ns.y, ns.x, ns.y};
+          const int src = ((min(g + 8 * mt, p.M - 1) - 8 * mt) << 2) | t4;
 #pragma unroll
-          for (int st = 0; st < 8; ++st) {
-            const uint32_t m = 0x00030003u << (2 * (st & 3));
-            const int w = 2 * (st >> 2);
-            mma_bf16_16816(c, wg[w] & m, wh[w] & m, wg[w + 1] & m, wh[w + 1] & m, bf[2 * st], bf[2 * st + 1]);
-          }
-          tot[mt][0] = fmaf(dg, c[0], tot[mt][0]);
-          tot[mt][1] = fmaf(dg, c[1], tot[mt][1]);
-          tot[mt][2] = fmaf(dh, c[2], tot[mt][2]);
-          tot[mt][3] = fmaf(dh, c[3], tot[mt][3]);
+          for (int q = 0; q < 4; ++q) act[mt][q] = abuf[(mt * 4 + q) * 32 + src];
         }
-      };
-      block(std::integral_constant<int, 0>{});
-      block(std::integral_constant<int, 1>{});
-      block(std::integral_constant<int, 2>{});
-      block(std::integral_constant<int, 3>{});
+        __syncwarp();                               // read before the next copies are issued
+      }
+      // B fragments of the block (permuted, pre-scaled) and the -S chain.
+      uint32_t bf[MT][16];
+      float2 ns[MT];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const uint32_t r[16] = {act[mt][0].x, act[mt][0].y, act[mt][0].z, act[mt][0].w,
+                                act[mt][1].x, act[mt][1].y, act[mt][1].z, act[mt][1].w,
+                                act[mt][2].x, act[mt][2].y, act[mt][2].z, act[mt][2].w,
+                                act[mt][3].x, act[mt][3].y, act[mt][3].z, act[mt][3].w};
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const int x = st & 3, o = 8 * (st >> 2) + (x >> 1);
+          const uint32_t sel = (x & 1) ? 0x7632u : 0x5410u;
+          bf[mt][2 * st] = mul_bf16x2(__byte_perm(r[o], r[o + 4], sel), prescale(x));
+          bf[mt][2 * st + 1] = mul_bf16x2(__byte_perm(r[o + 2], r[o + 6], sel), prescale(x));
+        }
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const uint32_t no = neg_ones(st & 3);
+          mma_bf16_16816(c, no, no, no, no, bf[mt][2 * st], bf[mt][2 * st + 1]);
+        }
+        ns[mt] = make_float2(c[0], c[1]);           // the same for rows g and g + 8
+      }
+      if (kMulti && t + 1 < T) load_act(t + 1);   // the buffer was read above
+      const int s = t % SW;
+      if (live) live = tc::wait_or_abort(full0 + 8 * s, (t / SW) & 1, p.err, abort_flag);
+      live = __all_sync(0xFFFFFFFFu, live);
+      if (live) {
+        const uint8_t* blk = smem + L::kRawOff + s * kStageBytes + g * kRowBytes + 34 * b;
+#pragma unroll
+        for (int rt = 0; rt < kTiles; ++rt) {
+          const uint8_t* rg = blk + 16 * rt * kRowBytes;
+          const uint8_t* rh = rg + 8 * kRowBytes;
+          uint32_t wg0, wg1, wh0, wh1;
+          load_codes<kA>(rg, t4, wg0, wg1);
+          load_codes<kA>(rh, t4, wh0, wh1);
+          const float dg = load_d(rg), dh = load_d(rh);
+          const uint32_t wg[4] = {wg0, wg0 >> 8, wg1, wg1 >> 8};
+          const uint32_t wh[4] = {wh0, wh0 >> 8, wh1, wh1 >> 8};
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            float c[4] = {ns[mt].x, ns[mt].y, ns[mt].x, ns[mt].y};
+#pragma unroll
+            for (int st = 0; st < 8; ++st) {
+              const uint32_t m = 0x00030003u << (2 * (st & 3));
+              const int w = 2 * (st >> 2);
+              mma_bf16_16816(c, wg[w] & m, wh[w] & m, wg[w + 1] & m, wh[w + 1] & m, bf[mt][2 * st],
+                             bf[mt][2 * st + 1]);
+            }
+            tot[rt][mt][0] = fmaf(dg, c[0], tot[rt][mt][0]);
+            tot[rt][mt][1] = fmaf(dg, c[1], tot[rt][mt][1]);
+            tot[rt][mt][2] = fmaf(dh, c[2], tot[rt][mt][2]);
+            tot[rt][mt][3] = fmaf(dh, c[3], tot[rt][mt][3]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
-    if (kMulti && t + 1 < T)
-      asm volatile("bar.sync 1, %0;" ::"r"(kCompute * 32) : "memory");   // B buffer free for t + 1
-  }
+  };
+  if (b & 1)
+    run(std::integral_constant<int, 1>{});
+  else if (b & 2)
+    run(std::integral_constant<int, 2>{});
+  else
+    run(std::integral_constant<int, 0>{});
 
   // ------------------------------------------------------------ reduce + store
-  // The second half of each tile hands its partial sums to the first through
-  // shared memory (one named barrier per tile) and leaves; the first half
-  // adds them (first + second). Ranks 1.. then send their sums to rank 0,
-  // slot rank - 1 in this thread's fragment order, and leave; rank 0 adds
-  // the slots in rank order and stores.
-  float4* pair = reinterpret_cast<float4*>(smem + L::kPairOff) + rt * MT * 32 + lane;
-  if (half == 1) {
+  // The 8 warps' sums (one block each) are added in warp order through
+  // shared memory laid over the consumed raw buffers. Ranks 1.. send the
+  // result to rank 0 (slot rank - 1) with st.async and leave; rank 0 adds the
+  // slots in rank order and stores.
+  constexpr int kItems = kTiles * MT * 32;        // float4 items of one warp's sums
+  float4* red = reinterpret_cast<float4*>(smem + L::kRedOff);
+  asm volatile("bar.sync 1, %0;" ::"r"(kCompute * 32) : "memory");   // raw buffers consumed
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) pair[mt * 32] = make_float4(tot[mt][0], tot[mt][1], tot[mt][2], tot[mt][3]);
-    asm volatile("bar.arrive %0, 64;" ::"r"(2 + rt) : "memory");
-    return;
-  }
-  asm volatile("bar.sync %0, 64;" ::"r"(2 + rt) : "memory");
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    const float4 v = pair[mt * 32];
-    tot[mt][0] += v.x;
-    tot[mt][1] += v.y;
-    tot[mt][2] += v.z;
-    tot[mt][3] += v.w;
-  }
-  if (rank != 0) {
-    const uint32_t dst = tc::mapa_shared(
-        smem_u32(smem + L::kRecvOff + (rank - 1) * L::kRecvSlot + (rt * MT * 32 + lane) * 16), 0);
-    const uint32_t bar0 = tc::mapa_shared(recv_bar, 0);
+  for (int rt = 0; rt < kTiles; ++rt)
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
-      st_async_f4(dst + mt * 32 * 16, tot[mt][0], tot[mt][1], tot[mt][2], tot[mt][3], bar0);
+      red[warp * kItems + (rt * MT + mt) * 32 + lane] =
+          make_float4(tot[rt][mt][0], tot[rt][mt][1], tot[rt][mt][2], tot[rt][mt][3]);
+  asm volatile("bar.sync 1, %0;" ::"r"(kCompute * 32) : "memory");
+  const int item = threadIdx.x;                   // (tile, m tile, lane) of a warp's fragment
+  if (item >= kItems) return;
+  float4 v = red[item];
+#pragma unroll
+  for (int w = 1; w < kCompute; ++w) {            // warp (block) order
+    const float4 u = red[w * kItems + item];
+    v.x += u.x;
+    v.y += u.y;
+    v.z += u.z;
+    v.w += u.w;
+  }
+  if (rank != 0) {
+    const uint32_t dst = tc::mapa_shared(smem_u32(smem + L::kRecvOff + (rank - 1) * L::kSlot + item * 16), 0);
+    st_async_f4(dst, v.x, v.y, v.z, v.w, tc::mapa_shared(recv_bar, 0));
     return;
   }
   bool ok = splits == 1 || mbar_wait(recv_bar, 0, p.err);
-  ok = ok && live && *abort_flag == 0;
+  ok = ok && *abort_flag == 0;
   if (!ok) return;
+  const float4* recv = reinterpret_cast<const float4*>(smem + L::kRecvOff) + item;
+  for (int q = 1; q < splits; ++q) {              // rank order
+    const float4 u = recv[(q - 1) * kItems];
+    v.x += u.x;
+    v.y += u.y;
+    v.z += u.z;
+    v.w += u.w;
+  }
   const float kUnscale = __uint_as_float((127u + 69u) << 23);   // 2^69
-  const float4* recv = reinterpret_cast<const float4*>(smem + L::kRecvOff) + rt * MT * 32 + lane;
+  const int rt = item / (MT * 32), mt = (item / 32) % MT, ln = item % 32;
+  const int r = 16 * rt + (ln >> 2), m = 8 * mt + 2 * (ln & 3);
+  const float acc[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    float acc[4] = {tot[mt][0], tot[mt][1], tot[mt][2], tot[mt][3]};
-    for (int q = 1; q < splits; ++q) {            // rank order
-      const float4 v = recv[(q - 1) * (L::kRecvSlot / 16) + mt * 32];
-      acc[0] += v.x;
-      acc[1] += v.y;
-      acc[2] += v.z;
-      acc[3] += v.w;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = r0 + 8 * (i >> 1);
-      const int m = 8 * mt + 2 * t4 + (i & 1);
-      if (m < p.M && n0 + r < p.N) p.C[static_cast<size_t>(m) * p.ldc + n0 + r] = f32_to_bf16_rn(acc[i] * kUnscale);
-    }
+  for (int i = 0; i < 4; ++i) {
+    const int rr = r + 8 * (i >> 1), mm = m + (i & 1);
+    if (mm < p.M && n0 + rr < p.N) p.C[static_cast<size_t>(mm) * p.ldc + n0 + rr] = f32_to_bf16_rn(acc[i] * kUnscale);
   }
 }
 
