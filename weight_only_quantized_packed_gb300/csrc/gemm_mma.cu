@@ -2,42 +2,45 @@
 // (mma.sync m16n8k16, BF16 operands, FP32 accumulation), swap-AB: the MMA's
 // 16 "rows" are weight rows n, its 8 "columns" are activation rows m.
 //
-// What it computes is the Q2_0 product of "Ternary Bonsai 8B on GB10: Q2_0
-// GEMV" (format and formula sections):
+// What it computes is the ternary Q2_0 product of
+// "spark_model/layers/ops/gemv_q2_vec.rs" (module docs; the formula of the
+// test helper `gemv_row`):
 //   C[m, n] = bf16( sum_k A[m, k] * (c[n, k] - 1) * d[n, k / 128] ),
-// the same result as q2_gemm_tc, to the tensor-core tolerance (the MMA sums
-// 16 products in its own order; see the "FP8 M=16 tensor-core" section of
-// "Bonsai ternary / FP8 decode kernels: M-dispatch, tiers and tensor cores").
+// the same result as q2_gemm_tc, within the tensor-core tolerance of
+// "metrale_model_layers/layers/ops/w8a16_gemm_m16.rs" (module docs: the
+// tensor core reduces 16 K-products in its own order).
 //
 // Why registers instead of tensor memory: the GEMV is a weight stream, and
 // every weight must pass through the converter exactly once. Feeding tcgen05
 // through tensor memory puts a store -> commit -> barrier -> MMA -> commit ->
 // barrier round trip on every 128-K group; here each warp turns its own code
 // words into MMA operands in registers and issues the MMAs itself, so nothing
-// waits on another warp except the stage hand-off.
+// waits on another warp until the stage's sums are added.
 //
 // Layout of one CTA (BM = 64 weight rows x the CTA's K range):
-//   warps 0..7  compute: warp w owns rows 16 (w % 4) .. + 15 of the tile and
-//               blocks 4 (w / 4) .. + 3 of every stage (the two halves'
-//               partial sums are added in shared memory at the end);
+//   warps 0..7  compute: warp w owns block w (128 K) of every stage, for all
+//               four 16-row tiles of the CTA;
 //   warp 8      producer: TMA of raw stages (64 rows x 8 blocks x 34 bytes).
 // Per 128-K block b and thread (g = lane / 4, t = lane % 4):
-//   * A fragment: code words 2t and 2t + 1 of the block, rows g and g + 8.
-//     Word bits 2q..2q+1 hold code q (q < 16). The pair of 16-bit lanes
-//     (code x, code 8 + x), masked in place by (word & 0x00030003 << 2x), is
-//     the BF16 pair (c_x 4^x, c_{8+x} 4^x) * 2^-133 (a subnormal or the
-//     smallest normal, exact); (word >> 8) gives codes (4 + x, 12 + x).
+//   * A fragment: code words 2t and 2t + 1 of the block, rows g and g + 8 of
+//     a tile. Word bits 2q..2q+1 hold code q (q < 16). The pair of 16-bit
+//     lanes (code x, code 8 + x), masked in place by
+//     (word & 0x00030003 << 2x), is the BF16 pair (c_x 4^x, c_{8+x} 4^x) *
+//     2^-133 (a subnormal or the smallest normal, exact); (word >> 8) gives
+//     codes (4 + x, 12 + x).
 //   * B fragment: activation rows m = g (and g + 8 for M > 8): the 32
 //     activations of k = 128 b + 32 t .. + 31, paired the same way and
 //     multiplied by 2^(64 - 2x), so every product is c * a * 2^-69 exactly.
-//   * The chain starts from -2^-69 * sum_k a (an MMA chain with every code 1
-//     and a negative sign, run once per block by the warp that prepares that
-//     block's B fragments), so it ends at 2^-69 * sum_k (c - 1) a.
+//     Built once per block, in registers, and used for all four tiles.
+//   * Each tile's chain starts from -2^-69 * sum_k a (an MMA chain with every
+//     code 1 and a negative sign, run once per block), so it ends at
+//     2^-69 * sum_k (c - 1) a.
 //   * acc += d * chain, and C = bf16(acc * 2^69).
+// Reduction: the 8 warps' sums are added in warp order in shared memory.
 // Split-K: the CTAs of a cluster split the K stages. Rank 0 owns the tile:
-// every other rank sends its partial sums into rank 0's shared memory with
-// st.async (completing on an mbarrier of rank 0) and exits at once, freeing
-// its SM for the next grid; rank 0 adds them in rank order and stores.
+// every other rank sends its sums into rank 0's shared memory with st.async
+// (completing on an mbarrier of rank 0) and exits at once, freeing its SM
+// for the next grid; rank 0 adds them in rank order and stores.
 #include <atomic>
 #include <type_traits>
 
