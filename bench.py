@@ -25,6 +25,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -119,11 +120,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _code_only(text):
+    """Source text without comments and blank lines: a comment edit leaves
+    the compiled kernel, and so its recorded DRAM traffic, unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(l.rstrip() for l in text.splitlines() if l.strip())
+
+
 def source_hash(tc=False):
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[tc]:
-        with open(os.path.join(ROOT, "weight_only_quantized_packed_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "weight_only_quantized_packed_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
