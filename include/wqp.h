@@ -100,6 +100,8 @@ int q2_gemm_tc_strided(const void* A, int lda, const void* W, void* C, int ldc,
  * cluster and the partial sums are added in rank order in shared memory.
  * Arguments, layouts and limits are those of q2_gemm_tc (1 <= M <= 16,
  * K % 1024 == 0, |a| < 2^62); anything else gives WQP_ERR_INVALID_ARG.
+ * One launch serves 8 activation rows; M > 8 is two launches on the same
+ * stream (the weights are read twice).
  * Numerics: the contract of w8a16_gemm_tc. Not bit-identical to q2_gemv or
  * q2_gemm_tc. A row does not depend on the other rows of the call.
  * Device-side waits are bounded as for the other kernels (see

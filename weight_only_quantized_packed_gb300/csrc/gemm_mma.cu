@@ -1,4 +1,5 @@
-// Q2_0 GEMM for 1 <= M <= 16 on the warp-level tensor-core path
+// Q2_0 GEMM for 1 <= M <= 8 per launch (the C ABI splits M <= 16 into 8-row
+// launches) on the warp-level tensor-core path
 // (mma.sync m16n8k16, BF16 operands, FP32 accumulation), swap-AB: the MMA's
 // 16 "rows" are weight rows n, its 8 "columns" are activation rows m.
 //
@@ -28,7 +29,7 @@
 //     (word & 0x00030003 << 2x), is the BF16 pair (c_x 4^x, c_{8+x} 4^x) *
 //     2^-133 (a subnormal or the smallest normal, exact); (word >> 8) gives
 //     codes (4 + x, 12 + x).
-//   * B fragment: activation rows m = g (and g + 8 for M > 8): the 32
+//   * B fragment: activation row m = g (rows past M repeat row M - 1): the 32
 //     activations of k = 128 b + 32 t .. + 31, paired the same way and
 //     multiplied by 2^(64 - 2x), so every product is c * a * 2^-69 exactly.
 //     Built once per block, in registers, and used for all four tiles.
@@ -60,7 +61,8 @@ constexpr int kRowBytes = kBlocks * 34;      // 272: 17 x 16 bytes
 constexpr int kStageBytes = BM * kRowBytes;  // 17408
 constexpr int kMaxSplits = 8;                // CTAs per cluster (K split) at most (portable size)
 
-// MT: m tiles of 8 activation rows, 1 (M <= 8) or 2 (M <= 16).
+// MT: m tiles of 8 activation rows per launch (1 is the one launched: a
+// 16-row form measured slower than two 8-row launches).
 // kMulti: a CTA runs more than one raw stage (two raw buffers, one refilled
 // while the other is consumed); otherwise exactly one.
 template <int MT, bool kMulti>
@@ -266,69 +268,80 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 
   load_act(0);
   bool live = true;
+  // One m tile at a time: its B fragments and offset chain, then the four
+  // row tiles against them (for M > 8 the codes are decoded once per m tile,
+  // which keeps a single set of fragments live).
   auto run = [&](auto ac) {
     constexpr int kA = decltype(ac)::value;
     for (int t = 0; t < T; ++t) {
       if constexpr (kMulti) {
         cp_async_wait_all();                        // this thread's copies of stage t
         __syncwarp();                               // and the other lanes' (rows past M)
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const int src = ((min(g + 8 * mt, p.M - 1) - 8 * mt) << 2) | t4;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) act[mt][q] = abuf[(mt * 4 + q) * 32 + src];
-        }
-        __syncwarp();                               // read before the next copies are issued
       }
-      // B fragments of the block (permuted, pre-scaled) and the -S chain.
-      uint32_t bf[MT][16];
-      float2 ns[MT];
+      const int s = t % SW;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const uint32_t r[16] = {act[mt][0].x, act[mt][0].y, act[mt][0].z, act[mt][0].w,
-                                act[mt][1].x, act[mt][1].y, act[mt][1].z, act[mt][1].w,
-                                act[mt][2].x, act[mt][2].y, act[mt][2].z, act[mt][2].w,
-                                act[mt][3].x, act[mt][3].y, act[mt][3].z, act[mt][3].w};
+        uint32_t r[16];
+        if constexpr (kMulti) {
+          const int src = ((min(g + 8 * mt, p.M - 1) - 8 * mt) << 2) | t4;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = abuf[(mt * 4 + q) * 32 + src];
+            r[4 * q] = v.x;
+            r[4 * q + 1] = v.y;
+            r[4 * q + 2] = v.z;
+            r[4 * q + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            r[4 * q] = act[mt][q].x;
+            r[4 * q + 1] = act[mt][q].y;
+            r[4 * q + 2] = act[mt][q].z;
+            r[4 * q + 3] = act[mt][q].w;
+          }
+        }
+        // B fragments of the block (permuted, pre-scaled) and the -S chain.
+        uint32_t bf[16];
 #pragma unroll
         for (int st = 0; st < 8; ++st) {
           const int x = st & 3, o = 8 * (st >> 2) + (x >> 1);
           const uint32_t sel = (x & 1) ? 0x7632u : 0x5410u;
-          bf[mt][2 * st] = mul_bf16x2(__byte_perm(r[o], r[o + 4], sel), prescale(x));
-          bf[mt][2 * st + 1] = mul_bf16x2(__byte_perm(r[o + 2], r[o + 6], sel), prescale(x));
+          bf[2 * st] = mul_bf16x2(__byte_perm(r[o], r[o + 4], sel), prescale(x));
+          bf[2 * st + 1] = mul_bf16x2(__byte_perm(r[o + 2], r[o + 6], sel), prescale(x));
         }
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        float ns[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int st = 0; st < 8; ++st) {
           const uint32_t no = neg_ones(st & 3);
-          mma_bf16_16816(c, no, no, no, no, bf[mt][2 * st], bf[mt][2 * st + 1]);
+          mma_bf16_16816(ns, no, no, no, no, bf[2 * st], bf[2 * st + 1]);
         }
-        ns[mt] = make_float2(c[0], c[1]);           // the same for rows g and g + 8
-      }
-      if (kMulti && t + 1 < T) load_act(t + 1);   // the buffer was read above
-      const int s = t % SW;
-      if (live) live = tc::wait_or_abort(full0 + 8 * s, (t / SW) & 1, p.err, abort_flag);
-      live = __all_sync(0xFFFFFFFFu, live);
-      if (live) {
-        const uint8_t* blk = smem + L::kRawOff + s * kStageBytes + g * kRowBytes + 34 * b;
+        if (kMulti && mt == MT - 1 && t + 1 < T) {
+          __syncwarp();                             // every lane has read the buffer
+          load_act(t + 1);
+        }
+        if (mt == 0) {
+          if (live) live = tc::wait_or_abort(full0 + 8 * s, (t / SW) & 1, p.err, abort_flag);
+          live = __all_sync(0xFFFFFFFFu, live);
+        }
+        if (live) {
+          const uint8_t* blk = smem + L::kRawOff + s * kStageBytes + g * kRowBytes + 34 * b;
 #pragma unroll
-        for (int rt = 0; rt < kTiles; ++rt) {
-          const uint8_t* rg = blk + 16 * rt * kRowBytes;
-          const uint8_t* rh = rg + 8 * kRowBytes;
-          uint32_t wg0, wg1, wh0, wh1;
-          load_codes<kA>(rg, t4, wg0, wg1);
-          load_codes<kA>(rh, t4, wh0, wh1);
-          const float dg = load_d(rg), dh = load_d(rh);
-          const uint32_t wg[4] = {wg0, wg0 >> 8, wg1, wg1 >> 8};
-          const uint32_t wh[4] = {wh0, wh0 >> 8, wh1, wh1 >> 8};
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            float c[4] = {ns[mt].x, ns[mt].y, ns[mt].x, ns[mt].y};
+          for (int rt = 0; rt < kTiles; ++rt) {
+            const uint8_t* rg = blk + 16 * rt * kRowBytes;
+            const uint8_t* rh = rg + 8 * kRowBytes;
+            uint32_t wg0, wg1, wh0, wh1;
+            load_codes<kA>(rg, t4, wg0, wg1);
+            load_codes<kA>(rh, t4, wh0, wh1);
+            const float dg = load_d(rg), dh = load_d(rh);
+            const uint32_t wg[4] = {wg0, wg0 >> 8, wg1, wg1 >> 8};
+            const uint32_t wh[4] = {wh0, wh0 >> 8, wh1, wh1 >> 8};
+            float c[4] = {ns[0], ns[1], ns[0], ns[1]};   // rows g and g + 8 start alike
 #pragma unroll
             for (int st = 0; st < 8; ++st) {
               const uint32_t m = 0x00030003u << (2 * (st & 3));
               const int w = 2 * (st >> 2);
-              mma_bf16_16816(c, wg[w] & m, wh[w] & m, wg[w + 1] & m, wh[w + 1] & m, bf[mt][2 * st],
-                             bf[mt][2 * st + 1]);
+              mma_bf16_16816(c, wg[w] & m, wh[w] & m, wg[w + 1] & m, wh[w + 1] & m, bf[2 * st], bf[2 * st + 1]);
             }
             tot[rt][mt][0] = fmaf(dg, c[0], tot[rt][mt][0]);
             tot[rt][mt][1] = fmaf(dg, c[1], tot[rt][mt][1]);
@@ -533,8 +546,7 @@ cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   const int tiles = (a.N + BM - 1) / BM;
   p.splits = choose_splits(tiles, p.stages, a.num_sms);
   const bool multi = (p.stages + p.splits - 1) / p.splits > 1;
-  if (a.M > 8)
-    return multi ? launch_variant<2, true, 2>(mw, p, tiles, a.pdl, s) : launch_variant<2, false, 2>(mw, p, tiles, a.pdl, s);
+  // One 8-row activation tile (MT = 1): the C ABI calls this on 8-row chunks.
   if (multi) return launch_variant<1, true, 3>(mw, p, tiles, a.pdl, s);
   // Three CTAs per SM spread a grid that fits them over more SMs (the cluster
   // scheduler fills an SM's free slots before the next SM's); four only when
