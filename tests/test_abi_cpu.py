@@ -132,6 +132,28 @@ def test_validation_other_formats(L):
     assert L.w8a16_dequant(P16, NUL, P16b, 8, 128, S) == 1
 
 
+@pytest.mark.parametrize("name", ["q2_gemm_tc", "q2_gemm_mma"])
+def test_q2_tensor_core_validation(L, name):
+    """Both Q2_0 tensor-core entries: 1 <= M <= 16, K % 1024 == 0, 16-byte
+    aligned A and W, row pitches; rejected before any CUDA call."""
+    f = getattr(L, name)
+    fs = getattr(L, name + "_strided")
+    for m in (0, 17, -1):
+        assert f(P16, P16b, P16c, m, 8, 1024, S) == 1, m
+    for k in (640, 1152, 128):
+        assert f(P16, P16b, P16c, 1, 8, k, S) == 1, k
+        assert b"1024" in L.wqp_last_error(), k
+    assert f(ODD, P16b, P16c, 1, 8, 1024, S) == 1
+    assert f(P16, ODD, P16c, 1, 8, 1024, S) == 1
+    assert f(NUL, P16b, P16c, 1, 8, 1024, S) == 1
+    assert f(P16, P16b, P16c, 1, 0, 1024, S) == 1
+    # strided: lda < K, lda % 8, ldc < N
+    assert fs(P16, 1000, P16b, P16c, 8, 1, 8, 1024, S) == 1
+    assert fs(P16, 1028, P16b, P16c, 8, 1, 8, 1024, S) == 1
+    assert fs(P16, 1024, P16b, P16c, 7, 1, 8, 1024, S) == 1
+    assert name.encode() in L.wqp_last_error()
+
+
 def test_m_zero_is_a_noop(L):
     """M == 0 returns OK without touching CUDA (the page's empty chunk list)."""
     assert L.q2_gemv(P16, P16b, NUL, P16c, 0, 8, 128, S) == 0
