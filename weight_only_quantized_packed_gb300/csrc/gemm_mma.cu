@@ -54,7 +54,7 @@ namespace mma {
 
 constexpr int BM = 64;                       // weight rows per CTA
 constexpr int kTiles = 4;                    // 16-row MMA tiles per CTA
-constexpr int kCompute = 2 * kTiles;         // compute warps: two per tile, four blocks each
+constexpr int kCompute = 2 * kTiles;         // compute warps: one per 128-K block of a stage (8)
 constexpr int kThreads = (kCompute + 1) * 32;
 constexpr int kBlocks = 8;                   // 128-K blocks per raw stage (1024 K)
 constexpr int kRowBytes = kBlocks * 34;      // 272: 17 x 16 bytes
