@@ -125,7 +125,7 @@ def _code_only(text):
     the compiled kernel, and so its recorded DRAM traffic, unchanged."""
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
-    return "\n".join(l.rstrip() for l in text.splitlines() if l.strip())
+    return "\n".join(l.strip() for l in text.splitlines() if l.strip())
 
 
 def source_hash(tc=False):

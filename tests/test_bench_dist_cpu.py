@@ -56,3 +56,30 @@ def test_single_rank_identity():
 
     assert bench.reduce_max_ms(12.5, None) == 12.5
     assert bench.job_value(6_963_200, 100, 1, 1.0) == pytest.approx(6_963_200 * 100 / 1e-3 / 1e9)
+
+
+def test_traffic_key_ignores_comments_only():
+    """The recorded DRAM traffic is keyed on the kernel sources without
+    comments: a comment edit keeps the key, a code edit changes it."""
+    import bench
+
+    src = "int f(int x) {  // doubles x\n  /* block\n comment */ return 2 * x;\n}\n"
+    same = "// header\nint f(int x) {  // twice x\n\n  return 2 * x;\n}\n"
+    other = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(other)
+
+
+def test_committed_traffic_matches_current_sources():
+    """Every recorded tensor-core entry the headline can use is keyed on the
+    current sources (so the bench reports traffic, not null)."""
+    import json
+    import os
+
+    import bench
+
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        d = json.load(f)
+    key = f"{bench.Q2_PATH[bench.HEADLINE['tc'][8]]}_M8_N{bench.HEADLINE['N']}_K{bench.HEADLINE['K']}"
+    assert key in d
+    assert bench.committed_traffic(key, bench.HEADLINE["tc"][8]) == d[key]["dram_bytes_per_launch"]
