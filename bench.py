@@ -40,6 +40,7 @@ UNIT = "GB/s"
 # The step calls, for each M, the library's fastest Q2_0 path at this shape
 # (measured): the warp-level tensor-core GEMM (q2_gemm_mma) at M = 1, 4 and 8.
 HEADLINE = {"fmt": "q2", "N": 5120, "K": 5120, "Ms": (1, 4, 8), "tc": {1: "mma", 4: "mma", 8: "mma"}}
+WORKLOAD = "Q2_0 GEMV N=5120 K=5120, one step = M=1, 4, 8 calls"   # both arms' config
 KERNEL_SOURCES = {False: ["gemv_scalar.cuh", "gemv_q2.cu", "decode.cuh", "common.cuh"],
                   True: ["gemm_tc.cu", "tc.cuh", "decode.cuh", "common.cuh"],
                   "mma": ["gemm_mma.cu", "tc.cuh", "common.cuh"]}
@@ -417,7 +418,7 @@ def gpu_arm(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; A ~ N(0,1) bf16, ternary codes U{0,1,2}, d U[0.01,0.05] fp16)",
-        "config": {"workload": "Q2_0 GEMV N=5120 K=5120, one step = M=1, 4, 8 calls",
+        "config": {"workload": WORKLOAD,
                    "paths": {str(M): Q2_PATH[H["tc"][M]] for M in H["Ms"]},
                    "timing": f"CUDA graph of {G} steps replayed {args.steps // G} times",
                    "weight_bytes_per_call": w.wb, "weight_buffers_cycled": w.nbuf,
@@ -573,7 +574,7 @@ def reference_arm(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3 / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": f"q2_gemv N=5120 K=5120, one step = M=1, 4, 8 calls, sampled to {rows} rows"},
+            "config": {"workload": WORKLOAD},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.max_threads(),
                              "kind": "oracle", "sample": f"{rows} of {H['N']} rows per step"},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
