@@ -27,9 +27,11 @@
  *   - for the strided forms, lda >= K, lda % 8 == 0 and ldc >= N.
  * Device. The library is built for sm_103a only. Any other device returns
  *   WQP_ERR_UNSUPPORTED.
- * Rows. The GEMVs accept any M >= 0. Up to 16 rows go in one launch: every
- *   weight byte is read once for all of those rows. Larger M is served in
- *   16-row chunks, with A and C advanced by whole rows.
+ * Rows. Every compute entry accepts any M >= 0. Up to 16 rows go in one
+ *   launch: every weight byte is read once for all of those rows. Larger M is
+ *   served in 16-row launches on the same stream, with A and C advanced by
+ *   whole rows ("w8a16_gemm_m16.rs", doc of `w8a16_gemm_m16`: callers with
+ *   more rows than the M tile run it again on the next contiguous rows).
  * Numerics. A row of a batched call equals the same row computed with M = 1,
  *   bit for bit, and does not depend on the other rows. The tensor-core
  *   entries are exempt (see w8a16_gemm_tc).
@@ -81,11 +83,15 @@ int q2_gemv_strided(const void* A, int lda, const void* W, void* C, int ldc,
  * activations as a * 2^(64 - 2j), so every product c * a is exact; each
  * 128-K group's sum of (c - 1) * a is scaled by its inline d once, in FP32.
  * Activations must satisfy |a| < 2^62 (the pre-scale stays finite).
- * Arguments and layouts are those of q2_gemv, with two more limits:
- * 1 <= M <= 16, and K % 1024 == 0, so that rows stay 16-byte aligned for the
- * tensor-map copies. Anything else gives WQP_ERR_INVALID_ARG.
- * Numerics: the contract is that of w8a16_gemm_tc. It is not bit-identical
- * to q2_gemv. A row does not depend on the other rows of the call.
+ * Arguments and layouts are those of q2_gemv, with one more limit:
+ * K % 1024 == 0, so that rows stay 16-byte aligned for the tensor-map
+ * copies. Anything else gives WQP_ERR_INVALID_ARG.
+ * Numerics: every product is exact and only the order of the FP32 additions
+ * differs from the plain row sum, so the contract is the scalar one: within
+ * 1 BF16 ULP of the FP32 row sum, or within the FP32 reordering bound
+ * 8 * sqrt(K) * 2^-24 * sum_k |a * w| for outputs near zero. It is not
+ * bit-identical to q2_gemv. A row does not depend on the other rows of the
+ * call.
  */
 int q2_gemm_tc(const void* A, const void* W, void* C, int M, int N, int K, void* stream);
 int q2_gemm_tc_strided(const void* A, int lda, const void* W, void* C, int ldc,
@@ -98,12 +104,12 @@ int q2_gemm_tc_strided(const void* A, int lda, const void* W, void* C, int ldc,
  * a * 2^(64 - 2j)); each 128-K block's sum of (c - 1) * a is scaled by its
  * inline d once, in FP32. The K range is split over the CTAs of a thread-block
  * cluster and the partial sums are added in rank order in shared memory.
- * Arguments, layouts and limits are those of q2_gemm_tc (1 <= M <= 16,
- * K % 1024 == 0, |a| < 2^62); anything else gives WQP_ERR_INVALID_ARG.
+ * Arguments, layouts and limits are those of q2_gemm_tc (K % 1024 == 0,
+ * |a| < 2^62); anything else gives WQP_ERR_INVALID_ARG.
  * One launch serves 8 activation rows; M > 8 is two launches on the same
  * stream (the weights are read twice).
- * Numerics: the contract of w8a16_gemm_tc. Not bit-identical to q2_gemv or
- * q2_gemm_tc. A row does not depend on the other rows of the call.
+ * Numerics: the scalar contract of q2_gemm_tc. Not bit-identical to q2_gemv
+ * or q2_gemm_tc. A row does not depend on the other rows of the call.
  * Device-side waits are bounded as for the other kernels (see
  * wqp_get_device_error).
  */
@@ -134,12 +140,13 @@ int w4a16_gemv_ex(const void* A, int lda, const void* W, const void* scales,
  * the 128-row MMA side and the activation rows padded to 16 on the MMA N
  * side. Each e2m1 * e4m3 product is exact in BF16, so the products are
  * exact; the global scale multiplies each FP32 result once, at the store.
- * Arguments and layouts are those of w4a16_gemv / w4a16_gemv_ex, with two
- * more limits: 1 <= M <= 16, and K % 256 == 0, so that the scale rows
- * (K/16 bytes) are multiples of 16 bytes for the tensor-map copies. Anything
- * else gives WQP_ERR_INVALID_ARG.
- * Numerics: the contract is that of w8a16_gemm_tc. It is not bit-identical
- * to w4a16_gemv. A row does not depend on the other rows of the call.
+ * Arguments and layouts are those of w4a16_gemv / w4a16_gemv_ex, with one
+ * more limit: K % 256 == 0, so that the scale rows (K/16 bytes) are
+ * multiples of 16 bytes for the tensor-map copies. Anything else gives
+ * WQP_ERR_INVALID_ARG.
+ * Numerics: the products are exact, so the contract is the scalar one of
+ * q2_gemm_tc. It is not bit-identical to w4a16_gemv. A row does not depend
+ * on the other rows of the call.
  */
 int w4a16_gemm_tc(const void* A, const void* W, const void* scales, void* C,
                   int M, int N, int K, void* stream);
@@ -164,10 +171,9 @@ int w8a16_gemm_strided(const void* A, int lda, const void* W, const float* scale
 
 /* Tensor-core (tcgen05) form of w8a16_gemm: swap-AB, with the weights on the
  * 128-row MMA side and the activation rows padded to 16 on the MMA N side.
- * Same arguments and layouts as w8a16_gemm, but 1 <= M <= 16 (M outside
- * that range gives WQP_ERR_INVALID_ARG). This follows "w8a16_gemm_m16.rs",
- * doc of `w8a16_gemm_m16`: the kernel's M tile is 16 rows, and callers with
- * more rows split them.
+ * Same arguments and layouts as w8a16_gemm. The kernel's M tile is 16 rows
+ * ("w8a16_gemm_m16.rs", doc of `w8a16_gemm_m16`); M > 16 runs as further
+ * 16-row launches.
  * Numerics ("w8a16_gemm_m16.rs", module docs): the tensor core reduces each
  * 16-K step in its own order, so the result is not bit-identical to
  * w8a16_gemm. The contract is: at most 4 BF16 ULP from the reference, or an

@@ -16,6 +16,9 @@ Tolerances (stated once, used everywhere):
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -78,3 +81,38 @@ def assert_scalar_parity(gpu_bits, ref, K: int, what: str = ""):
             f"gpu={bf16_to_f64(gpu_bits[m, n])!r} oracle={bf16_to_f64(ref.c[m, n])!r} "
             f"ulp={bf16_ulp_dist(gpu_bits[m, n], ref.c[m, n])} S={ref.s[m, n]!r}")
     return only_floor
+
+
+def parity_report(gpu_bits, ref, K: int) -> dict:
+    """Counts behind the scalar term: outputs within 1 ULP, outputs that pass
+    only by the reordering floor, and the largest ULP distance."""
+    d = bf16_ulp_dist(gpu_bits, ref.c)
+    ok, only_floor = scalar_ok(gpu_bits, ref, K)
+    return {"n": int(d.size), "exact": int(np.count_nonzero(d == 0)), "le1ulp": int(np.count_nonzero(d <= 1)),
+            "floor_only": only_floor, "fail": int(np.count_nonzero(~ok)), "max_ulp": int(d.max()) if d.size else 0}
+
+
+# Outputs allowed to pass the scalar term only through the reordering floor
+# (the rest must be within 1 BF16 ULP): at most 2, or 0.2 % of the outputs.
+# Measured on GB300 over every parity case of the GPU tests: at most 1 in
+# 1040 outputs of a case, 0.02 % or less at the full-size shapes.
+FLOOR_ONLY_MAX_FRAC = 0.002
+FLOOR_ONLY_MIN_ALLOWED = 2
+
+
+def log_parity(what: str, rep: dict) -> None:
+    """Append one parity report as a JSON line to $WQP_PARITY_LOG, if set."""
+    path = os.environ.get("WQP_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": what, **rep}) + "\n")
+
+
+def assert_scalar_term(gpu_bits, ref, K: int, what: str = "") -> dict:
+    """Every output within the scalar term, the floor-only share bounded;
+    returns (and logs) the counts."""
+    rep = parity_report(gpu_bits, ref, K)
+    log_parity(what, rep)
+    assert_scalar_parity(gpu_bits, ref, K, what)
+    assert rep["floor_only"] <= max(FLOOR_ONLY_MIN_ALLOWED, FLOOR_ONLY_MAX_FRAC * rep["n"]), (what, rep)
+    return rep

@@ -8,7 +8,7 @@ import time
 import pytest
 
 from tests import _gpu as G
-from tests._tol import assert_scalar_parity
+from tests._tol import assert_scalar_term
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +42,7 @@ def test_bounded_wait_timeout_is_reported_and_context_stays_usable(oracle_lib):
     d = G.make("q2", 3, 64, 1024, seed=9)
     C = G.host_bits(G.run_gpu(d))
     ref = G.run_oracle(oracle_lib, d)
-    assert_scalar_parity(C, ref, 1024, "q2 after the timeout self-test")
+    assert_scalar_term(C, ref, 1024, "q2 after the timeout self-test")
 
 
 def test_selftest_rejects_bad_limits():

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from tests import _gpu as G
-from tests._tol import assert_scalar_parity, bf16_exact_bits, bf16_to_f64
+from tests._tol import assert_scalar_term, bf16_exact_bits, bf16_to_f64
 from weight_only_quantized_packed_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -45,7 +45,7 @@ def test_parity_small(oracle_lib, fmt, N, K):
         d = G.make(fmt, M, N, K, seed=1000 + N + K + M)
         C = G.host_bits(G.run_gpu(d))
         ref = G.run_oracle(oracle_lib, d)
-        assert_scalar_parity(C, ref, K, f"{fmt} M={M} N={N} K={K}")
+        assert_scalar_term(C, ref, K, f"{fmt} M={M} N={N} K={K}")
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -67,7 +67,7 @@ def test_m_above_16_is_chunked(oracle_lib, fmt):
         d = G.make(fmt, M, N, K, seed=5 + M)
         C = G.host_bits(G.run_gpu(d))
         ref = G.run_oracle(oracle_lib, d)
-        assert_scalar_parity(C, ref, K, f"{fmt} M={M}")
+        assert_scalar_term(C, ref, K, f"{fmt} M={M}")
         one = G.host_bits(G.run_gpu(d, A=d["dA"][M - 1:M]))
         assert np.array_equal(C[M - 1], one[0])
 
@@ -133,7 +133,7 @@ def test_strided_rows_and_canary(oracle_lib, fmt):
     assert (host[1:M + 1, N:] == -7.0).all()
     C = G.host_bits(canary[1:M + 1, :N].contiguous())
     ref = G.run_oracle(oracle_lib, d)
-    assert_scalar_parity(C, ref, K, f"{fmt} strided")
+    assert_scalar_term(C, ref, K, f"{fmt} strided")
 
 
 def test_dequant_bit_exact(oracle_lib):
@@ -178,7 +178,7 @@ def test_full_size_parity(oracle_lib, fmt, N, K, Ms):
         d = G.make(fmt, M, N, K, seed=synth.seed_for(7, M))
         C = G.host_bits(G.run_gpu(d))
         ref = G.run_oracle(oracle_lib, d)
-        assert_scalar_parity(C, ref, K, f"{fmt} full M={M} N={N} K={K}")
+        assert_scalar_term(C, ref, K, f"{fmt} full M={M} N={N} K={K}")
 
 
 @pytest.mark.parametrize("M", [1, 8])

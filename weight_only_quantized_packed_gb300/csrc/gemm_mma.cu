@@ -415,8 +415,6 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 }
 
 // ---------------------------------------------------------------- host side
-constexpr int kMaxDevices = 64;
-
 // The compiled variants: (m tiles, several stages per CTA, CTAs per SM).
 // Single-stage M <= 8 calls have two register budgets: 3 CTAs per SM (63
 // registers) and 4 (56 registers) for grids that need the fourth slot.
@@ -430,16 +428,8 @@ struct Variant {
 // occupancy query.
 template <int MT, bool kMulti, int kOcc>
 cudaError_t set_attrs() {
-  static std::atomic<int> done{0};
-  if (done.load(std::memory_order_acquire)) return cudaSuccess;
-  auto k = Variant<MT, kMulti, kOcc>::kernel;
-  cudaError_t e =
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MT, kMulti>::bytes(kMaxSplits));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
-  if (e == cudaSuccess) done.store(1, std::memory_order_release);
-  return e;
+  static AttrLatch latch;
+  return set_smem_attrs(Variant<MT, kMulti, kOcc>::kernel, latch, Cfg<MT, kMulti>::bytes(kMaxSplits), true);
 }
 
 // CTAs of a variant resident at once in clusters of s (0 if the query

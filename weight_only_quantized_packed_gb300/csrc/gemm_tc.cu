@@ -720,8 +720,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 // columns do run side by side, so cluster capacities are taken from this twin.
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) tc_capacity_twin() {}
 
-constexpr int kMaxDevices = 64;
-
 // Clusters of s CTAs (1 <= s <= 8) of format F that are resident at once on
 // the current device (0 if the query failed). Cached per device.
 template <class F>
@@ -780,16 +778,9 @@ cudaError_t launch_tc_nb(const CUtensorMap& mw, const CUtensorMap& mw2, const CU
                          int tiles, bool pdl,
                          cudaStream_t s) {
   using L = Layout<F>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_kernel<F, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    // Two CTAs per SM need the whole shared-memory carveout.
-    e = cudaFuncSetAttribute(tc_kernel<F, NB>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // Two CTAs per SM need the whole shared-memory carveout.
+  static AttrLatch latch;
+  if (cudaError_t e0 = set_smem_attrs(tc_kernel<F, NB>, latch, L::kAlloc, true); e0 != cudaSuccess) return e0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * p.splits);
   cfg.blockDim = dim3(kThreads);

@@ -314,12 +314,8 @@ template <class F, int M, bool BULK, bool ARES>
 cudaError_t launch_scalar_m(const GemvArgs& a, cudaStream_t s) {
   using Cfg = ScalarCfg<F, M, ARES>;
   auto kern = gemv_scalar_kernel<F, M, BULK, ARES>;
-  static bool attr_set = false;  // idempotent; racing writers set the same value
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemMax);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static AttrLatch latch;
+  if (cudaError_t e0 = set_smem_attrs(kern, latch, Cfg::kSmemMax, false); e0 != cudaSuccess) return e0;
   const int smem = Cfg::kSmemFixed + (ARES ? M * a.K * 4 : 0);
   CUtensorMap mw = {}, mw2 = {}, ma = {};
   cudaError_t e = cudaSuccess;

@@ -1,11 +1,40 @@
 // Internal launch interface between the C-ABI layer (abi.cu) and the kernel
 // translation units. Not installed; the public surface is include/wqp.h.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace wqp {
+
+// Devices a process may use with the per-device caches below.
+constexpr int kMaxDevices = 64;
+
+// Per-device latch for kernel attributes. cudaFuncSetAttribute acts on the
+// current device's context, so the opt-in above 48 KB of dynamic shared
+// memory (and the carveout) is set once per device, not once per process.
+struct AttrLatch {
+  std::atomic<int> done[kMaxDevices];
+};
+
+// Sets the dynamic shared-memory limit of `kernel` to `bytes` (and, when
+// asked, the largest shared-memory carveout) on the current device, once.
+// Racing callers may both set it; the values are the same.
+template <typename Kern>
+cudaError_t set_smem_attrs(Kern kernel, AttrLatch& latch, int bytes, bool max_carveout) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (latch.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && max_carveout)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  if (e == cudaSuccess) latch.done[dev].store(1, std::memory_order_release);
+  return e;
+}
 
 // Bits of the device error word.
 constexpr unsigned WQP_DEV_ERR_TIMEOUT = 1u;
