@@ -105,6 +105,17 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = A * B + c with a separate accumulator input (the first MMA of a chain
+// starts from c without copying it).
+__device__ __forceinline__ void mma_bf16_16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1, float c0, float c1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%10,%11};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
+
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -325,28 +336,47 @@ __global__ void __launch_bounds__(kThreads, kOcc)
           live = __all_sync(0xFFFFFFFFu, live);
         }
         if (live) {
+          // Two row tiles at a time: their MMA chains are independent, so one
+          // waits while the other issues.
           const uint8_t* blk = smem + L::kRawOff + s * kStageBytes + g * kRowBytes + 34 * b;
 #pragma unroll
-          for (int rt = 0; rt < kTiles; ++rt) {
-            const uint8_t* rg = blk + 16 * rt * kRowBytes;
-            const uint8_t* rh = rg + 8 * kRowBytes;
-            uint32_t wg0, wg1, wh0, wh1;
-            load_codes<kA>(rg, t4, wg0, wg1);
-            load_codes<kA>(rh, t4, wh0, wh1);
-            const float dg = load_d(rg), dh = load_d(rh);
-            const uint32_t wg[4] = {wg0, wg0 >> 8, wg1, wg1 >> 8};
-            const uint32_t wh[4] = {wh0, wh0 >> 8, wh1, wh1 >> 8};
-            float c[4] = {ns[0], ns[1], ns[0], ns[1]};   // rows g and g + 8 start alike
+          for (int r0 = 0; r0 < kTiles; r0 += 2) {
+            uint32_t wg[2][2], wh[2][2];           // code words 2t, 2t + 1 of rows g, g + 8
+            float dg[2], dh[2], c[2][4];
 #pragma unroll
-            for (int st = 0; st < 8; ++st) {
-              const uint32_t m = 0x00030003u << (2 * (st & 3));
-              const int w = 2 * (st >> 2);
-              mma_bf16_16816(c, wg[w] & m, wh[w] & m, wg[w + 1] & m, wh[w + 1] & m, bf[2 * st], bf[2 * st + 1]);
+            for (int i = 0; i < 2; ++i) {
+              const uint8_t* rg = blk + 16 * (r0 + i) * kRowBytes;
+              const uint8_t* rh = rg + 8 * kRowBytes;
+              load_codes<kA>(rg, t4, wg[i][0], wg[i][1]);
+              load_codes<kA>(rh, t4, wh[i][0], wh[i][1]);
+              dg[i] = load_d(rg);
+              dh[i] = load_d(rh);
             }
-            tot[rt][mt][0] = fmaf(dg, c[0], tot[rt][mt][0]);
-            tot[rt][mt][1] = fmaf(dg, c[1], tot[rt][mt][1]);
-            tot[rt][mt][2] = fmaf(dh, c[2], tot[rt][mt][2]);
-            tot[rt][mt][3] = fmaf(dh, c[3], tot[rt][mt][3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {          // code word 2t + h: codes 16h .. 16h + 15 of the block
+              const uint32_t sg[2] = {wg[0][h] >> 8, wg[1][h] >> 8};
+              const uint32_t sh[2] = {wh[0][h] >> 8, wh[1][h] >> 8};
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                const int st = 4 * h + x;
+                const uint32_t m = 0x00030003u << (2 * x);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                  const uint32_t a0 = wg[i][h] & m, a1 = wh[i][h] & m, a2 = sg[i] & m, a3 = sh[i] & m;
+                  if (st == 0)                     // rows g and g + 8 start alike, from the offset
+                    mma_bf16_16816_c(c[i], a0, a1, a2, a3, bf[0], bf[1], ns[0], ns[1]);
+                  else
+                    mma_bf16_16816(c[i], a0, a1, a2, a3, bf[2 * st], bf[2 * st + 1]);
+                }
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              tot[r0 + i][mt][0] = fmaf(dg[i], c[i][0], tot[r0 + i][mt][0]);
+              tot[r0 + i][mt][1] = fmaf(dg[i], c[i][1], tot[r0 + i][mt][1]);
+              tot[r0 + i][mt][2] = fmaf(dh[i], c[i][2], tot[r0 + i][mt][2]);
+              tot[r0 + i][mt][3] = fmaf(dh[i], c[i][3], tot[r0 + i][mt][3]);
+            }
           }
         }
       }
@@ -392,7 +422,10 @@ __global__ void __launch_bounds__(kThreads, kOcc)
     st_async_f4(dst, v.x, v.y, v.z, v.w, tc::mapa_shared(recv_bar, 0));
     return;
   }
-  bool ok = splits == 1 || mbar_wait(recv_bar, 0, p.err);
+  // Every peer sends, even one whose own waits gave up (each of those is
+  // bounded by kWaitLimitNs), so rank 0 waits three times as long: it never
+  // leaves while a peer may still write into its shared memory.
+  bool ok = splits == 1 || mbar_wait_ns(recv_bar, 0, p.err, 3 * kWaitLimitNs);
   ok = ok && *abort_flag == 0;
   if (!ok) return;
   const float4* recv = reinterpret_cast<const float4*>(smem + L::kRecvOff) + item;
@@ -519,8 +552,8 @@ cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   using namespace mma;
   const uint64_t G = static_cast<uint64_t>(a.K / 128);
   CUtensorMap mw;
-  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),
-                              34 * G, kBlocks * 17, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+  cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),
+                                34 * G, kBlocks * 17, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   MmaParams p;
   p.A = static_cast<const uint16_t*>(a.A);

@@ -837,7 +837,7 @@ cudaError_t launch_tc(const GemvArgs& a, const CUtensorMap& mw, const CUtensorMa
 cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s) {
   using namespace tc;
   CUtensorMap mw;
-  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, static_cast<uint64_t>(a.K),
+  cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, static_cast<uint64_t>(a.K),
                               static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K), GK, BM,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
@@ -851,7 +851,7 @@ cudaError_t launch_q2_gemm_tc(const GemvArgs& a, cudaStream_t s) {
   using namespace tc;
   const uint64_t G = static_cast<uint64_t>(a.K / GK);
   CUtensorMap mw;
-  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),
+  cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),
                               34 * G, 8 * 17, Q2Tc::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   return launch_tc<Q2Tc>(a, mw, mw, s);
@@ -864,10 +864,10 @@ cudaError_t launch_w4a16_gemm_tc(const GemvArgs& a, cudaStream_t s) {
   using namespace tc;
   const uint64_t K = static_cast<uint64_t>(a.K);
   CUtensorMap mw, ms;
-  cudaError_t e = make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, K / 2, static_cast<uint64_t>(a.N), K / 2,
+  cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, K / 2, static_cast<uint64_t>(a.N), K / 2,
                               128, W4Tc::kRows, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  e = make_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, K / 16, static_cast<uint64_t>(a.N), K / 16, 16,
+  e = cached_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, K / 16, static_cast<uint64_t>(a.N), K / 16, 16,
                   W4Tc::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   return launch_tc<W4Tc>(a, mw, ms, s);

@@ -80,6 +80,12 @@ cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                         CUtensorMapSwizzle sw);
 
+// Same, through a per-process cache keyed by every argument and the device
+// (weight maps: encoding one costs about as much host time as a launch).
+cudaError_t cached_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle sw);
+
 // Launch helper: programmatic stream serialization when pdl is set.
 template <typename Kern, typename... Args>
 cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,

@@ -40,6 +40,59 @@ cudaError_t make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+namespace {
+// Encoded maps keyed by everything they encode (and the device). A map holds
+// only the address, shape, pitch and box, so a cached one stays valid for
+// any buffer later placed at the same address.
+struct MapKey {
+  int dev;
+  CUtensorMapDataType dt;
+  const void* base;
+  uint64_t inner, outer, row_bytes;
+  uint32_t box_inner, box_outer;
+  CUtensorMapSwizzle sw;
+  bool operator==(const MapKey& o) const {
+    return dev == o.dev && dt == o.dt && base == o.base && inner == o.inner && outer == o.outer &&
+           row_bytes == o.row_bytes && box_inner == o.box_inner && box_outer == o.box_outer && sw == o.sw;
+  }
+};
+constexpr int kMapCache = 128;
+struct MapCache {
+  std::mutex mu;
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  int n = 0, next = 0;
+};
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+}  // namespace
+
+cudaError_t cached_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                          uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const MapKey k{dev, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw};
+  MapCache& c = map_cache();
+  {
+    std::lock_guard<std::mutex> lk(c.mu);
+    for (int i = 0; i < c.n; ++i)
+      if (c.key[i] == k) {
+        *m = c.map[i];
+        return cudaSuccess;
+      }
+  }
+  e = make_map_2d(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(c.mu);
+  const int i = c.n < kMapCache ? c.n++ : (c.next++ % kMapCache);
+  c.key[i] = k;
+  c.map[i] = *m;
+  return cudaSuccess;
+}
+
 cudaError_t make_act_map(CUtensorMap* m, const GemvArgs& a, int box_k) {
   // BF16 pairs as u32: K/2 columns, M rows, pitch lda * 2 bytes.
   return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.A, static_cast<uint64_t>(a.K / 2),
