@@ -214,10 +214,14 @@ class Workload:
             wqp.q2_gemm_tc(A, self.W[j], self.N, self.K, out=C)
         elif self.fmt == "q2":
             wqp.q2_gemv(A, self.W[j], self.N, self.K, out=C)
+        elif self.fmt == "w4" and tc == "mma":
+            wqp.w4a16_gemm_mma(A, self.W[j], self.S[j], self.N, self.K, out=C)
         elif self.fmt == "w4" and tc:
             wqp.w4a16_gemm_tc(A, self.W[j], self.S[j], self.N, self.K, out=C)
         elif self.fmt == "w4":
             wqp.w4a16_gemv(A, self.W[j], self.S[j], self.N, self.K, out=C)
+        elif tc == "mma":
+            wqp.w8a16_gemm_mma(A, self.W[j], self.S[j], self.N, self.K, out=C)
         elif tc:
             wqp.w8a16_gemm_tc(A, self.W[j], self.S[j], self.N, self.K, out=C)
         else:

@@ -154,6 +154,27 @@ int w4a16_gemm_tc_ex(const void* A, int lda, const void* W, const void* scales,
                      float global_scale, void* C, int ldc,
                      int M, int N, int K, void* stream);
 
+/* Warp-level tensor-core form of w4a16_gemv (mma.sync m16n8k16, FP16
+ * operands, FP32 accumulation), swap-AB with 16 weight rows by 8 activation
+ * rows per MMA (two column tiles for M = 9..16, so the weights are read once
+ * for up to 16 rows). The weight operand is e2m1 * e4m3(scale), exact in
+ * FP16. Each activation row is scaled per 128-K block by the power of two
+ * 2^e that puts its largest magnitude in [2^14, 2^15) and rounded to FP16
+ * (exact for every value of at least 2^-31 times that maximum); each block's
+ * FP32 sum is multiplied by 2^-e once, and the global scale multiplies each
+ * FP32 result at the store.
+ * Arguments and layouts are those of w4a16_gemv / w4a16_gemv_ex, with one
+ * more limit: K % 1024 == 0 (whole stages of 8 blocks for the tensor-map
+ * copies). Anything else gives WQP_ERR_INVALID_ARG.
+ * Numerics: the scalar contract of q2_gemm_tc. A row does not depend on the
+ * other rows of the call.
+ */
+int w4a16_gemm_mma(const void* A, const void* W, const void* scales, void* C,
+                   int M, int N, int K, void* stream);
+int w4a16_gemm_mma_ex(const void* A, int lda, const void* W, const void* scales,
+                      float global_scale, void* C, int ldc,
+                      int M, int N, int K, void* stream);
+
 /* ---------------------------------------------------------------- W8A16 ---
  * FP8 E4M3 weights with FP32 128x128 block scales, scalar-FMA decode GEMM.
  * Defined by "metrale_model_layers/layers/ops/w8a16_gemm_m16.rs" (doc of
@@ -184,6 +205,24 @@ int w8a16_gemm_tc(const void* A, const void* W, const float* scales, void* C,
                   int M, int N, int K, void* stream);
 int w8a16_gemm_tc_strided(const void* A, int lda, const void* W, const float* scales,
                           void* C, int ldc, int M, int N, int K, void* stream);
+
+/* Warp-level tensor-core form of w8a16_gemm (mma.sync m16n8k16, FP16
+ * operands, FP32 accumulation), swap-AB as w4a16_gemm_mma. E4M3 is a subset
+ * of FP16, so the weight operand is exact; the activations are scaled per
+ * (row, 128-K block) by a power of two and rounded to FP16 as in
+ * w4a16_gemm_mma. Each 128-K block's FP32 sum is multiplied once by its block
+ * scale (and by 2^-e) and added to the FP32 accumulator, as "w8a16_gemm_m16.rs"
+ * (module docs) requires.
+ * Arguments and layouts are those of w8a16_gemm, with two more limits:
+ * K % 1024 == 0, and scales 16-byte aligned (the tensor-map copies).
+ * Anything else gives WQP_ERR_INVALID_ARG.
+ * Numerics: the scalar contract of q2_gemm_tc. A row does not depend on the
+ * other rows of the call.
+ */
+int w8a16_gemm_mma(const void* A, const void* W, const float* scales, void* C,
+                   int M, int N, int K, void* stream);
+int w8a16_gemm_mma_strided(const void* A, int lda, const void* W, const float* scales,
+                           void* C, int ldc, int M, int N, int K, void* stream);
 
 /* ------------------------------------------------------------ dequant ---
  * Unpack every weight to FP32: out is float [N, K] row-major, device memory,

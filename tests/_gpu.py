@@ -52,10 +52,14 @@ def run_gpu(d, tc: bool = False, A=None, out=None):
         C = wqp.q2_gemm_tc(A, d["dW"], N, K, out=out)
     elif d["fmt"] == "q2":
         C = wqp.q2_gemv(A, d["dW"], N, K, out=out)
+    elif d["fmt"] == "w4" and tc == "mma":
+        C = wqp.w4a16_gemm_mma(A, d["dW"], d["dS"], N, K, d.get("g", 1.0), out=out)
     elif d["fmt"] == "w4" and tc:
         C = wqp.w4a16_gemm_tc(A, d["dW"], d["dS"], N, K, d.get("g", 1.0), out=out)
     elif d["fmt"] == "w4":
         C = wqp.w4a16_gemv(A, d["dW"], d["dS"], N, K, d.get("g", 1.0), out=out)
+    elif tc == "mma":
+        C = wqp.w8a16_gemm_mma(A, d["dW"], d["dS"], N, K, out=out)
     elif tc:
         C = wqp.w8a16_gemm_tc(A, d["dW"], d["dS"], N, K, out=out)
     else:

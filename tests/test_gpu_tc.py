@@ -39,10 +39,11 @@ def _lib():
 
 
 def _check_tc(oracle_lib, d, C, what):
-    """Q2_0 / W4: the scalar term on every output. FP8: the tensor-core term,
-    and the share within the scalar term is returned."""
+    """Q2_0, W4 and the FP8 warp-level MMA path: the scalar term on every
+    output. FP8 on tcgen05: the tensor-core term, and the share within the
+    scalar term is returned."""
     ref = G.run_oracle(oracle_lib, d)
-    if d["fmt"] in ("q2", "w4"):
+    if d["fmt"] in ("q2", "w4") or "mma" in what:
         assert_scalar_term(C, ref, d["K"], what)
         return 1.0
     a = synth.bf16_bits_to_f32(d["A"]).astype(np.float64)
@@ -344,4 +345,129 @@ def test_tc_m_above_16(oracle_lib, fmt, eng, K):
         _check_tc(oracle_lib, d, C, f"{fmt} {eng} M={M}")
         for m in (0, 16, M - 1):
             one = G.host_bits(G.run_gpu(d, tc=eng, A=d["dA"][m:m + 1]))
+            assert np.array_equal(one[0], C[m]), (M, m)
+
+
+# ------------------------------------------ FP8 and W4 on the warp-level MMA
+# w8a16_gemm_mma and w4a16_gemm_mma: FP16 operands, exact weights, activations
+# scaled per (row, 128-K block) by a power of two; held to the scalar term.
+F16_FMTS = pytest.mark.parametrize("fmt", ["w8", "w4"])
+
+
+@F16_FMTS
+@pytest.mark.parametrize("N,K", [(128, 1024), (200, 2048), (1000, 1024), (77, 3072), (384, 8192)])
+def test_f16_mma_parity_small(oracle_lib, fmt, N, K):
+    for M in (1, 5, 8, 16):
+        d = G.make(fmt, M, N, K, seed=1300 + N + K + M)
+        C = G.host_bits(G.run_gpu(d, tc="mma"))
+        _check_tc(oracle_lib, d, C, f"{fmt} mma M={M} N={N} K={K}")
+
+
+@F16_FMTS
+def test_f16_mma_exact_arithmetic_bit_exact(oracle_lib, fmt):
+    """Small-integer activations and power-of-two scales: every partial sum
+    is exact, so the MMA path gives the oracle's bits."""
+    r = np.random.default_rng(13)
+    M, N, K = 16, 260, 3072
+    A = synth.bf16_bits_from_f32(r.integers(-4, 5, size=(M, K)).astype(np.float32))
+    d = {"A": A, "dA": G.dev_bf16(A), "M": M, "N": N, "K": K, "fmt": fmt}
+    if fmt == "w8":
+        W = synth.e4m3_round(r.integers(-16, 17, size=(N, K)) / 8.0)
+        S = (2.0 ** r.integers(-2, 3, size=((N + 127) // 128, K // 128))).astype(np.float32)
+        d.update(W=W, S=S, dW=G.dev_u8(W), dS=G.dev_f32(S))
+    else:
+        nib = r.integers(0, 16, size=(N, K), dtype=np.uint8)
+        W = synth.pack_w4(nib)
+        S = synth.e4m3_round(2.0 ** r.integers(-2, 3, size=(N, K // 16)))
+        d.update(W=W, S=S, dW=G.dev_u8(W), dS=G.dev_u8(S), g=1.0)
+    C = G.host_bits(G.run_gpu(d, tc="mma"))
+    assert np.array_equal(C, G.run_oracle(oracle_lib, d).c)
+
+
+@F16_FMTS
+def test_f16_mma_one_hot_and_order(oracle_lib, fmt):
+    """One-hot activations pick single weights: each output is the dequantised
+    weight (times the block scale for FP8), bit for bit, at k positions that
+    cover every lane and MMA step of a block."""
+    N, K = 136, 2048
+    d0 = G.make(fmt, 1, N, K, seed=77)
+    if fmt == "w8":
+        deq = oracle_lib.w8_dequant(d0["W"], d0["S"], N, K)
+    else:
+        deq = oracle_lib.w4_dequant(d0["W"], d0["S"], 1.0, N, K)
+    for j in (0, 1, 2, 3, 4, 17, 31, 32, 63, 100, 127, 128, 1023, 1024, 2047):
+        A = np.zeros((2, K), np.float32)
+        A[0, j] = 1.0
+        A[1, j] = -0.5
+        Ab = synth.bf16_bits_from_f32(A)
+        d = dict(d0, A=Ab, dA=G.dev_bf16(Ab), M=2)
+        C = G.host_bits(G.run_gpu(d, tc="mma"))
+        exp = np.stack([deq[:, j], -0.5 * deq[:, j]]).astype(np.float64) + 0.0   # a zero weight gives +0
+        assert np.array_equal(C, bf16_exact_bits(exp)), j
+
+
+@F16_FMTS
+def test_f16_mma_activation_range(oracle_lib, fmt):
+    """The per-block power-of-two scaling of the activations keeps large,
+    small and mixed-magnitude rows within the scalar term."""
+    M, N, K = 4, 300, 2048
+    for scale in (2.0 ** 40, 2.0 ** -40, 1.0):
+        d = G.make(fmt, M, N, K, seed=81)
+        A = synth.bf16_bits_to_f32(d["A"]).astype(np.float64) * scale
+        if scale == 1.0:                          # one row spanning 2^-30 .. 2^30 within a block
+            A[1] *= 2.0 ** np.linspace(-30, 30, K)
+        Ab = synth.bf16_bits_from_f32(A.astype(np.float32))
+        d = dict(d, A=Ab, dA=G.dev_bf16(Ab))
+        C = G.host_bits(G.run_gpu(d, tc="mma"))
+        _check_tc(oracle_lib, d, C, f"{fmt} mma activation scale {scale:g}")
+
+
+def test_w4_mma_global_scale(oracle_lib):
+    d = G.make("w4", 5, 300, 1024, seed=31)
+    d["g"] = 0.37109375
+    C = G.host_bits(G.run_gpu(d, tc="mma"))
+    _check_tc(oracle_lib, d, C, "w4 mma global scale")
+
+
+@F16_FMTS
+def test_f16_mma_rows_independent_and_k_rule(fmt):
+    import weight_only_quantized_packed_gb300 as wqp
+
+    d = G.make(fmt, 16, 5120, 5120, seed=23)
+    c16 = G.host_bits(G.run_gpu(d, tc="mma"))
+    assert np.array_equal(c16, G.host_bits(G.run_gpu(d, tc="mma")))   # deterministic
+    for m in (0, 8, 15):
+        one = G.host_bits(G.run_gpu(d, tc="mma", A=d["dA"][m:m + 1]))
+        assert np.array_equal(one[0], c16[m])
+    bad = G.make(fmt, 1, 64, 640 if fmt == "w8" else 768, seed=3)
+    with pytest.raises(wqp.WqpError):
+        G.run_gpu(bad, tc="mma")                 # K % 1024 != 0
+
+
+@pytest.mark.parametrize("fmt,N,K,Ms", [("w8", 17408, 5120, (1, 8, 16)), ("w8", 5120, 17408, (2, 16)),
+                                        ("w4", 5120, 5120, (1, 8, 16)), ("w4", 17408, 5120, (4,))])
+def test_f16_mma_full_size(oracle_lib, fmt, N, K, Ms):
+    for M in Ms:
+        d = G.make(fmt, M, N, K, seed=synth.seed_for(3 if fmt == "w8" else 2, M))
+        C = G.host_bits(G.run_gpu(d, tc="mma"))
+        _check_tc(oracle_lib, d, C, f"{fmt} mma full M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("fmt,N,K", [("w8", 200, 2048), ("w8", 1000, 5120), ("w4", 200, 2048), ("w4", 77, 4096)])
+def test_f16_mma_strided_rows_and_canary(oracle_lib, fmt, N, K):
+    for M in (5, 16):
+        d = G.make(fmt, M, N, K, seed=51 + M + N)
+        C = _strided_canary(oracle_lib, d, "mma", K + 64, N + 13, f"{fmt} mma strided M={M} N={N} K={K}")
+        assert np.array_equal(C, G.host_bits(G.run_gpu(d, tc="mma")))
+
+
+@F16_FMTS
+def test_f16_mma_m_above_16(oracle_lib, fmt):
+    N, K = 300, 2048
+    for M in (17, 32):
+        d = G.make(fmt, M, N, K, seed=950 + M)
+        C = G.host_bits(G.run_gpu(d, tc="mma"))
+        _check_tc(oracle_lib, d, C, f"{fmt} mma M={M}")
+        for m in (0, 16, M - 1):
+            one = G.host_bits(G.run_gpu(d, tc="mma", A=d["dA"][m:m + 1]))
             assert np.array_equal(one[0], C[m]), (M, m)

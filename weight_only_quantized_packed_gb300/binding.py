@@ -12,7 +12,8 @@ import os
 import threading
 
 __all__ = [
-    "WqpError", "lib", "lib_path", "q2_gemv", "q2_gemm_tc", "q2_gemm_mma", "w4a16_gemv", "w4a16_gemm_tc", "w8a16_gemm", "w8a16_gemm_tc",
+    "WqpError", "lib", "lib_path", "q2_gemv", "q2_gemm_tc", "q2_gemm_mma", "w4a16_gemv", "w4a16_gemm_tc",
+    "w4a16_gemm_mma", "w8a16_gemm", "w8a16_gemm_tc", "w8a16_gemm_mma",
     "q2_dequant", "w4a16_dequant", "w8a16_dequant", "row_chunks", "set_pdl",
     "get_device_error", "selftest_wait_timeout", "status_string", "EXPORTS", "MAX_M_PER_LAUNCH",
 ]
@@ -37,10 +38,14 @@ EXPORTS = {
     "w4a16_gemv_ex": [_P, _I, _P, _P, _F, _P, _I, _I, _I, _I, _P],
     "w4a16_gemm_tc": [_P, _P, _P, _P, _I, _I, _I, _P],
     "w4a16_gemm_tc_ex": [_P, _I, _P, _P, _F, _P, _I, _I, _I, _I, _P],
+    "w4a16_gemm_mma": [_P, _P, _P, _P, _I, _I, _I, _P],
+    "w4a16_gemm_mma_ex": [_P, _I, _P, _P, _F, _P, _I, _I, _I, _I, _P],
     "w8a16_gemm": [_P, _P, _P, _P, _I, _I, _I, _P],
     "w8a16_gemm_strided": [_P, _I, _P, _P, _P, _I, _I, _I, _I, _P],
     "w8a16_gemm_tc": [_P, _P, _P, _P, _I, _I, _I, _P],
     "w8a16_gemm_tc_strided": [_P, _I, _P, _P, _P, _I, _I, _I, _I, _P],
+    "w8a16_gemm_mma": [_P, _P, _P, _P, _I, _I, _I, _P],
+    "w8a16_gemm_mma_strided": [_P, _I, _P, _P, _P, _I, _I, _I, _I, _P],
     "q2_dequant": [_P, _P, _I, _I, _P],
     "w4a16_dequant": [_P, _P, _F, _P, _I, _I, _P],
     "w8a16_dequant": [_P, _P, _P, _I, _I, _P],
@@ -182,6 +187,26 @@ def w4a16_gemm_tc(A, W, scales, N: int, K: int, global_scale: float = 1.0, out=N
     C = _out(A, M, N, out)
     _check(lib().w4a16_gemm_tc_ex(_ptr(A), lda, _ptr(W), _ptr(scales), float(global_scale), _ptr(C),
                                   C.stride(0), M, N, K, _stream(stream)), "w4a16_gemm_tc")
+    return C
+
+
+def w4a16_gemm_mma(A, W, scales, N: int, K: int, global_scale: float = 1.0, out=None, stream=None):
+    """Warp-level tensor-core (mma.sync swap-AB) form of w4a16_gemv, K % 1024 == 0."""
+    _need_cuda(A, W, scales, out)
+    M, lda = _rows(A, K)
+    C = _out(A, M, N, out)
+    _check(lib().w4a16_gemm_mma_ex(_ptr(A), lda, _ptr(W), _ptr(scales), float(global_scale), _ptr(C),
+                                   C.stride(0), M, N, K, _stream(stream)), "w4a16_gemm_mma")
+    return C
+
+
+def w8a16_gemm_mma(A, W, scales, N: int, K: int, out=None, stream=None):
+    """Warp-level tensor-core (mma.sync swap-AB) form of w8a16_gemm, K % 1024 == 0."""
+    _need_cuda(A, W, scales, out)
+    M, lda = _rows(A, K)
+    C = _out(A, M, N, out)
+    _check(lib().w8a16_gemm_mma_strided(_ptr(A), lda, _ptr(W), _ptr(scales), _ptr(C), C.stride(0),
+                                        M, N, K, _stream(stream)), "w8a16_gemm_mma")
     return C
 
 

@@ -80,7 +80,7 @@ int device_setup(DeviceInfo** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-enum class Fmt { Q2, W4, W8, W8TC, Q2TC, W4TC, Q2MMA };
+enum class Fmt { Q2, W4, W8, W8TC, Q2TC, W4TC, Q2MMA, W8MMA, W4MMA };
 
 const char* fmt_name(Fmt f) {
   switch (f) {
@@ -91,6 +91,8 @@ const char* fmt_name(Fmt f) {
     case Fmt::Q2TC: return "q2_gemm_tc";
     case Fmt::W4TC: return "w4a16_gemm_tc";
     case Fmt::Q2MMA: return "q2_gemm_mma";
+    case Fmt::W8MMA: return "w8a16_gemm_mma";
+    case Fmt::W4MMA: return "w4a16_gemm_mma";
   }
   return "?";
 }
@@ -99,13 +101,13 @@ int validate(Fmt f, const void* A, int lda, const void* W, const void* scales, v
              int M, int N, int K) {
   const char* nm = fmt_name(f);
   if (M < 0) return fail(WQP_ERR_INVALID_ARG, "%s: M=%d < 0", nm, M);
-  const bool w4 = (f == Fmt::W4 || f == Fmt::W4TC);
+  const bool w4 = (f == Fmt::W4 || f == Fmt::W4TC || f == Fmt::W4MMA);
   const bool q2 = (f == Fmt::Q2 || f == Fmt::Q2TC || f == Fmt::Q2MMA);
   if (N < 1 || N > (1 << 24)) return fail(WQP_ERR_INVALID_ARG, "%s: N=%d outside 1..2^24", nm, N);
   if (K < 128 || K > (1 << 20) || K % 128 != 0)
     return fail(WQP_ERR_INVALID_ARG, "%s: K=%d must be a multiple of 128 in [128, 2^20]", nm, K);
   if (!A || !W || !C) return fail(WQP_ERR_INVALID_ARG, "%s: NULL A, W or C", nm);
-  if ((f == Fmt::Q2TC || f == Fmt::Q2MMA) && K % 1024 != 0)
+  if ((f == Fmt::Q2TC || f == Fmt::Q2MMA || f == Fmt::W8MMA || f == Fmt::W4MMA) && K % 1024 != 0)
     return fail(WQP_ERR_INVALID_ARG, "%s: K=%d must be a multiple of 1024", nm, K);
   if (f == Fmt::W4TC && K % 256 != 0)
     return fail(WQP_ERR_INVALID_ARG, "%s: K=%d must be a multiple of 256", nm, K);
@@ -118,6 +120,8 @@ int validate(Fmt f, const void* A, int lda, const void* W, const void* scales, v
     return fail(WQP_ERR_INVALID_ARG, "%s: scales must be 16-byte aligned", nm);
   if ((f == Fmt::W8 || f == Fmt::W8TC) && !aligned(scales, 4))
     return fail(WQP_ERR_INVALID_ARG, "%s: scales must be 4-byte aligned", nm);
+  if (f == Fmt::W8MMA && !aligned(scales, 16))
+    return fail(WQP_ERR_INVALID_ARG, "%s: scales must be 16-byte aligned", nm);
   if (!aligned(C, 2)) return fail(WQP_ERR_INVALID_ARG, "%s: C must be 2-byte aligned", nm);
   if (lda < K || lda % 8 != 0)
     return fail(WQP_ERR_INVALID_ARG, "%s: lda=%d must be >= K=%d and a multiple of 8", nm, lda, K);
@@ -129,7 +133,7 @@ int run_gemm(Fmt f, const void* A, int lda, const void* W, const void* scales, f
              void* C, int ldc, int M, int N, int K, void* stream) {
   int st = validate(f, A, lda, W, scales, C, ldc, M, N, K);
   if (st != WQP_OK) return st;
-  if ((f == Fmt::W4 || f == Fmt::W4TC) && !(gscale == gscale))
+  if ((f == Fmt::W4 || f == Fmt::W4TC || f == Fmt::W4MMA) && !(gscale == gscale))
     return fail(WQP_ERR_INVALID_ARG, "%s: global_scale is NaN", fmt_name(f));
   if (M == 0) return WQP_OK;
   DeviceInfo* dev = nullptr;
@@ -163,6 +167,8 @@ int run_gemm(Fmt f, const void* A, int lda, const void* W, const void* scales, f
       case Fmt::Q2TC: e = launch_q2_gemm_tc(a, s); break;
       case Fmt::W4TC: e = launch_w4a16_gemm_tc(a, s); break;
       case Fmt::Q2MMA: e = launch_q2_gemm_mma(a, s); break;
+      case Fmt::W8MMA: e = launch_w8a16_gemm_mma(a, s); break;
+      case Fmt::W4MMA: e = launch_w4a16_gemm_mma(a, s); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, fmt_name(f));
   }
@@ -265,6 +271,26 @@ int w4a16_gemm_tc(const void* A, const void* W, const void* scales, void* C, int
 int w4a16_gemm_tc_ex(const void* A, int lda, const void* W, const void* scales, float global_scale,
                      void* C, int ldc, int M, int N, int K, void* stream) {
   return run_gemm(Fmt::W4TC, A, lda, W, scales, global_scale, C, ldc, M, N, K, stream);
+}
+
+int w4a16_gemm_mma(const void* A, const void* W, const void* scales, void* C, int M, int N, int K,
+                   void* stream) {
+  return run_gemm(Fmt::W4MMA, A, K, W, scales, 1.0f, C, N, M, N, K, stream);
+}
+
+int w4a16_gemm_mma_ex(const void* A, int lda, const void* W, const void* scales, float global_scale,
+                      void* C, int ldc, int M, int N, int K, void* stream) {
+  return run_gemm(Fmt::W4MMA, A, lda, W, scales, global_scale, C, ldc, M, N, K, stream);
+}
+
+int w8a16_gemm_mma(const void* A, const void* W, const float* scales, void* C, int M, int N, int K,
+                   void* stream) {
+  return run_gemm(Fmt::W8MMA, A, K, W, scales, 1.0f, C, N, M, N, K, stream);
+}
+
+int w8a16_gemm_mma_strided(const void* A, int lda, const void* W, const float* scales, void* C,
+                           int ldc, int M, int N, int K, void* stream) {
+  return run_gemm(Fmt::W8MMA, A, lda, W, scales, 1.0f, C, ldc, M, N, K, stream);
 }
 
 int w8a16_gemm(const void* A, const void* W, const float* scales, void* C, int M, int N, int K,

@@ -198,6 +198,26 @@ __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// Cluster barrier halves: an early relaxed arrive at entry (every rank's
+// barriers are initialised before anyone writes into a peer), its wait
+// before the first remote operation.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// Four floats into a CTA's shared memory through a shared::cluster address,
+// completing as 16 bytes on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+               : "memory");
+}
+// Arrive on an mbarrier of a CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // Bounded mbarrier wait that also gives up early when another role of the
 // CTA has already aborted (flag in shared memory).
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, unsigned* err,
@@ -206,6 +226,33 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uns
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_flag) return false;
+    if (wait_expired(i, t0, kWaitLimitNs)) break;
+  }
+  set_error(err, WQP_DEV_ERR_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+// Phase test that acquires at cluster scope (the phase is completed by an
+// arrive from another CTA of the cluster), bounded like wait_or_abort.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, unsigned* err,
+                                                      volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((i & 255u) == 255u && *abort_flag) return false;
     if (wait_expired(i, t0, kWaitLimitNs)) break;
   }
