@@ -167,13 +167,26 @@ def test_q2_tc_rows_independent_and_k_rule(eng):
 
 
 @pytest.mark.parametrize("N,K,Ms", [(5120, 5120, (1, 4, 8, 16)), (7168, 5120, (8,)),
-                                    (5120, 17408, (16,)), (34816, 5120, (4,))])
+                                    (5120, 17408, (16,)), (34816, 5120, (4, 16))])
 @ENGINES
 def test_q2_tc_full_size(oracle_lib, N, K, Ms, eng):
     for M in Ms:
         d = G.make("q2", M, N, K, seed=synth.seed_for(1, M))
         C = G.host_bits(G.run_gpu(d, tc=eng))
         _check_tc(oracle_lib, d, C, f"q2 full M={M} N={N} K={K} {eng}")
+
+
+def test_q2_mma_persistent_rows_independent():
+    """The dense-FFN gate+up shape runs on the persistent kernel: a row of a
+    16-row call (two column tiles, weights read once) equals the row computed
+    alone, and a 12-row call gives the same rows."""
+    d = G.make("q2", 16, 34816, 5120, seed=24)
+    c16 = G.host_bits(G.run_gpu(d, tc="mma"))
+    c12 = G.host_bits(G.run_gpu(d, tc="mma", A=d["dA"][:12]))
+    assert np.array_equal(c12, c16[:12])
+    for m in (0, 9, 15):
+        one = G.host_bits(G.run_gpu(d, tc="mma", A=d["dA"][m:m + 1]))
+        assert np.array_equal(one[0], c16[m]), m
 
 
 @ENGINES
@@ -430,10 +443,11 @@ def test_w4_mma_global_scale(oracle_lib):
 
 
 @F16_FMTS
-def test_f16_mma_rows_independent_and_k_rule(fmt):
+@pytest.mark.parametrize("N", [5120, 17408])
+def test_f16_mma_rows_independent_and_k_rule(fmt, N):
     import weight_only_quantized_packed_gb300 as wqp
 
-    d = G.make(fmt, 16, 5120, 5120, seed=23)
+    d = G.make(fmt, 16, N, 5120, seed=23)
     c16 = G.host_bits(G.run_gpu(d, tc="mma"))
     assert np.array_equal(c16, G.host_bits(G.run_gpu(d, tc="mma")))   # deterministic
     for m in (0, 8, 15):

@@ -150,10 +150,7 @@ int run_gemm(Fmt f, const void* A, int lda, const void* W, const void* scales, f
   a.err = dev->err;
   a.num_sms = dev->num_sms;
   a.pdl = g_pdl.load(std::memory_order_relaxed) != 0;
-  // q2_gemm_mma runs one 8-row activation tile per launch: M > 8 is two
-  // launches (measured faster than one 16-row kernel, and each row's result
-  // is the one an M <= 8 call gives).
-  const int step = f == Fmt::Q2MMA ? 8 : WQP_MAX_M_PER_LAUNCH;
+  const int step = WQP_MAX_M_PER_LAUNCH;
   for (int r0 = 0; r0 < M; r0 += step) {
     a.M = (M - r0) < step ? (M - r0) : step;
     a.A = static_cast<const char*>(A) + static_cast<size_t>(r0) * lda * 2;

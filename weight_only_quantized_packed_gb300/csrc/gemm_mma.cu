@@ -550,6 +550,20 @@ cudaError_t launch_variant(const CUtensorMap& mw, const MmaParams& p, int tiles,
 // boundary (the TMA box's x = 136 * stage elements of 2 bytes).
 cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   using namespace mma;
+  // At least two 64-row tiles per SM: the persistent kernel (weights read once
+  // for up to 16 rows; B fragments built once per CTA). Otherwise one short
+  // CTA per (tile, stage range) and 8 activation rows per launch. The choice
+  // depends on the shape only, so a row's result does not depend on M.
+  if ((a.N + BM - 1) / BM >= 2 * a.num_sms) return launch_q2_gemm_stream(a, s);
+  if (a.M > 8) {
+    GemvArgs lo = a, hi = a;
+    lo.M = 8;
+    hi.M = a.M - 8;
+    hi.A = static_cast<const uint16_t*>(a.A) + static_cast<size_t>(8) * a.lda;
+    hi.C = static_cast<uint16_t*>(a.C) + static_cast<size_t>(8) * a.ldc;
+    const cudaError_t e1 = launch_q2_gemm_mma(lo, s);
+    return e1 != cudaSuccess ? e1 : launch_q2_gemm_mma(hi, s);
+  }
   const uint64_t G = static_cast<uint64_t>(a.K / 128);
   CUtensorMap mw;
   cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),

@@ -632,9 +632,10 @@ void consider(Plan& best, int splits, int tiles, int stages, int num_sms) {
 // busiest SM's work. It depends on N, K and the device, never on the
 // activation rows, so a row's result does not depend on the other rows.
 template <class F, int MT>
-Plan choose_plan(int tiles, int stages, int num_sms) {
+Plan choose_plan(int tiles, int stages, int num_sms, int only_splits = 0) {
   Plan best;
   for (int s = 1; s <= kMaxSplits && s <= stages; ++s) {
+    if (only_splits > 0 && s != only_splits) continue;
     if (s == stages) {
       // Two column tiles need more registers than two CTAs per SM leave.
       if constexpr (MT == 1) consider<F, 1, true, 2>(best, s, tiles, stages, num_sms);
@@ -712,7 +713,11 @@ cudaError_t launch_fmt(const GemvArgs& a, const CUtensorMap& mw, const CUtensorM
       }
   }
   if (!have) {
-    pl = mt == 1 ? choose_plan<F, 1>(tiles, stages, a.num_sms) : choose_plan<F, 2>(tiles, stages, a.num_sms);
+    // The K split (and so every row's summation order) is the one of the
+    // 8-row plan for every M, so a row's result does not depend on how many
+    // rows the call has.
+    pl = choose_plan<F, 1>(tiles, stages, a.num_sms);
+    if (pl.cost >= 0 && mt == 2) pl = choose_plan<F, 2>(tiles, stages, a.num_sms, pl.splits);
     std::lock_guard<std::mutex> lk(pc.mu);
     const int i = pc.n < kPlanCache ? pc.n++ : (pc.next++ % kPlanCache);
     pc.key[i] = key;

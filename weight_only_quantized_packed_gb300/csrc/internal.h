@@ -68,6 +68,7 @@ cudaError_t launch_w8a16_gemm(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_q2_gemm_tc(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s);
+cudaError_t launch_q2_gemm_stream(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_w4a16_gemm_tc(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_w8a16_gemm_mma(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_w4a16_gemm_mma(const GemvArgs& a, cudaStream_t s);
