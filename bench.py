@@ -43,7 +43,9 @@ HEADLINE = {"fmt": "q2", "N": 5120, "K": 5120, "Ms": (1, 4, 8), "tc": {1: "mma",
 WORKLOAD = "Q2_0 GEMV N=5120 K=5120, one step = M=1, 4, 8 calls"   # both arms' config
 KERNEL_SOURCES = {False: ["gemv_scalar.cuh", "gemv_q2.cu", "decode.cuh", "common.cuh"],
                   True: ["gemm_tc.cu", "tc.cuh", "decode.cuh", "common.cuh"],
-                  "mma": ["gemm_mma.cu", "tc.cuh", "common.cuh"]}
+                  "mma": ["gemm_mma.cu", "tc.cuh", "common.cuh"],
+                  "stream": ["gemm_mma_stream.cu", "tc.cuh", "common.cuh"],
+                  "f16": ["gemm_mma_f16.cu", "tc.cuh", "decode.cuh", "common.cuh"]}
 # Q2_0 entry point per path key (False: scalar, True: tcgen05, "mma": mma.sync).
 Q2_PATH = {False: "q2_gemv", True: "q2_gemm_tc", "mma": "q2_gemm_mma"}
 
@@ -54,6 +56,16 @@ def weight_bytes(fmt, N, K):
 
     return {"q2": synth.q2_weight_bytes, "w4": synth.w4_weight_bytes,
             "w8": synth.w8_weight_bytes}[fmt](N, K)
+
+
+def peak_bf16():
+    """Measured dense bf16 tensor throughput (TFLOP/s, burst), else the
+    fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
 
 
 def peaks():
@@ -275,38 +287,79 @@ def time_calls(fn, n, warm=3, reps=3):
     return statistics.median(out)
 
 
-def sweep(l2, peak):
-    """us/call and GB/s for every workload (one line each), PDL on."""
+# Per-SM pipe rates measured on GB300 with microbenchmarks (lane operations
+# or instructions per SM clock), used for the compute view of each line:
+# LOP3/PRMT/SHF/IMAD and the packed f16/bf16 multiplies 64, FFMA 128,
+# mma.sync m16n8k16 0.5 (and it does not overlap the ALU pipe), the
+# E4M3/E2M1 -> f16x2 conversions 32.
+PIPE = {"alu": 64.0, "ffma": 128.0, "mma": 0.5, "cvt": 32.0}
+# Decode work per weight of each warp-level MMA engine: (ALU lane-ops, cvt lane-ops).
+MMA_DECODE = {"q2": (0.5625, 0.0), "w4": (0.5, 0.5), "w8": (0.0, 0.5)}
+
+
+def compute_view(fmt, path, N, K, M, us, sm_count, f_mhz, bf16_tflops):
+    """The engine's compute bound next to the HBM one: the time its pipes
+    need at the measured per-SM rates, as a fraction of the call's time."""
+    cyc = us * 1e-6 * f_mhz * 1e6            # SM clocks of the call
+    w = float(N) * K                         # weights
+    if path == "mma":
+        alu, cvt = MMA_DECODE[fmt]
+        mmas = w / 256.0 * ((M + 7) // 8)
+        need = (w * alu / PIPE["alu"] + w * cvt / PIPE["cvt"] + mmas / PIPE["mma"]) / sm_count
+        return {"engine": "mma.sync", "pipe_bound_us": round(need / (f_mhz * 1e6) * 1e6, 3),
+                "frac": round(need / cyc, 4),
+                "model": f"per SM: {alu} ALU + {cvt} cvt lane-ops per weight, {(M + 7) // 8} mma per 256 weights, "
+                         "ALU and tensor pipes not overlapping"}
+    if path is True:
+        flops = 2.0 * 16 * N * K              # M padded to 16 on the MMA's N side
+        return {"engine": "tcgen05", "tensor_tflops": round(flops / (us * 1e-6) / 1e12, 2),
+                "frac": round(flops / (us * 1e-6) / 1e12 / bf16_tflops, 4),
+                "model": "dense bf16 tensor rate (measured cuBLAS peak)"}
+    fmas = w * M
+    return {"engine": "scalar FFMA", "fma_tflops": round(fmas / (us * 1e-6) / 1e12, 3),
+            "frac": round(fmas / cyc / (PIPE["ffma"] * sm_count), 4),
+            "model": f"{sm_count} SMs x 128 FP32 lanes x {f_mhz:.0f} MHz"}
+
+
+def sweep(l2, peak, sm_count, f_mhz, bf16_tflops):
+    """us/call, GB/s, HBM fraction and compute view for every workload and
+    engine (one line each), PDL on."""
     import torch
 
     import weight_only_quantized_packed_gb300 as wqp
 
     out = []
+    names = {("q2", False): "q2_gemv", ("q2", True): "q2_gemm_tc", ("q2", "mma"): "q2_gemm_mma",
+             ("w4", False): "w4a16_gemv", ("w4", True): "w4a16_gemm_tc", ("w4", "mma"): "w4a16_gemm_mma",
+             ("w8", False): "w8a16_gemm", ("w8", True): "w8a16_gemm_tc", ("w8", "mma"): "w8a16_gemm_mma"}
     specs = [
-        ("q2_gemv N=256 K=512", "q2", 256, 512, (1,), False, 0),
-        ("q2_gemv N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), False, 1),
-        ("q2_gemm_tc N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), True, 1),
-        ("q2_gemm_mma N=5120 K=5120", "q2", 5120, 5120, (1, 4, 8, 16), "mma", 1),
-        ("w4a16_gemv N=5120 K=5120", "w4", 5120, 5120, tuple(range(1, 9)), False, 2),
-        ("w4a16_gemm_tc N=5120 K=5120", "w4", 5120, 5120, (1, 4, 8, 16), True, 2),
-        ("w8a16_gemm N=17408 K=5120", "w8", 17408, 5120, (1, 4, 8, 16), False, 3),
-        ("w8a16_gemm N=5120 K=17408", "w8", 5120, 17408, (1, 4, 8, 16), False, 3),
-        ("w8a16_gemm_tc N=17408 K=5120", "w8", 17408, 5120, (1, 8, 16), True, 3),
-        ("w8a16_gemm_tc N=5120 K=17408", "w8", 5120, 17408, (1, 8, 16), True, 3),
+        ("q2", 256, 512, (1,), False, 0),
+        ("q2", 5120, 5120, (1, 4, 8, 16), False, 1),
+        ("q2", 5120, 5120, (1, 4, 8, 16), True, 1),
+        ("q2", 5120, 5120, (1, 4, 8, 16), "mma", 1),
+        ("w4", 5120, 5120, tuple(range(1, 9)), False, 2),
+        ("w4", 5120, 5120, (1, 4, 8, 16), True, 2),
+        ("w4", 5120, 5120, tuple(range(1, 9)) + (16,), "mma", 2),
+        ("w8", 17408, 5120, (1, 4, 8, 16), False, 3),
+        ("w8", 5120, 17408, (1, 4, 8, 16), False, 3),
+        ("w8", 17408, 5120, (1, 8, 16), True, 3),
+        ("w8", 5120, 17408, (1, 8, 16), True, 3),
+        ("w8", 17408, 5120, (1, 8, 16), "mma", 3),
+        ("w8", 5120, 17408, (1, 8, 16), "mma", 3),
     ]
     wqp.set_pdl(True)
     try:
-        for name, fmt, N, K, Ms, tc, wl in specs:
+        for fmt, N, K, Ms, tc, wl in specs:
             w = Workload(fmt, N, K, Ms, l2, wl, tc=tc)
             for M in Ms:
                 us = time_calls(lambda: w.call(M), max(20, min(400, int(2e5 / max(1, w.wb // 4096)))))
                 gbs = w.wb / us / 1e3
-                out.append({"workload": name, "M": M, "us": round(us, 3), "gbs": round(gbs, 1),
-                            "pct_peak": round(100 * gbs / peak, 1)})
+                out.append({"workload": f"{names[(fmt, tc)]} N={N} K={K}", "M": M, "us": round(us, 3),
+                            "gbs": round(gbs, 1), "pct_peak": round(100 * gbs / peak, 1),
+                            "compute_view": compute_view(fmt, tc, N, K, M, us, sm_count, f_mhz, bf16_tflops)})
             w.free()
             torch.cuda.empty_cache()
-        # Decoder-layer sequence: qkv, o, gate+up, down, 8 layers cycled;
-        # tensor core at every M (the faster path on each of these shapes).
+        # Decoder-layer sequence: qkv, o, gate+up, down, 8 layers cycled.
         layer = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
         ws = [Workload("q2", N, K, (1, 4, 8, 16), 0, 4, cap_bytes=0) for (N, K) in layer]
         for w in ws:
@@ -369,18 +422,27 @@ def gpu_arm(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
+        # REPS timed regions, each of exactly `steps` steps bracketed by a
+        # synchronize (and a barrier across ranks); the line reports their
+        # median and spread.
         stream = steps_graph.stream
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.steps // G):
-                steps_graph.replay()
-            e1.record(stream)
-        e1.synchronize()
+        reps_ms = []
+        for _ in range(args.reps):
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(args.steps // G):
+                    steps_graph.replay()
+                e1.record(stream)
+            e1.synchronize()
+            reps_ms.append(e0.elapsed_time(e1))
         if dist:
             dist.barrier()
-        ms_total = e0.elapsed_time(e1)
+        ms_total = statistics.median(reps_ms)
         # Per-kernel durations: each call of the step alone, as a graph of
         # back-to-back calls (events on the launching stream around it).
         avg = {M: time_calls(lambda M=M: w.call(M, tc=H["tc"][M]), 200) for M in H["Ms"]}
@@ -401,16 +463,14 @@ def gpu_arm(args, rank, world, local_rank):
                 "kernel": f"{kname} M={Mdom} N={H['N']} K={H['K']}",
                 "algorithmic_bytes_per_launch": w.wb,
                 "traffic": committed_traffic(f"{kname}_M{Mdom}_N{H['N']}_K{H['K']}", tc_dom)}
-    # ALU view of the same kernel: useful FMAs per second over the FP32 FMA peak.
+    # Compute view of the same kernel: the time its pipes need at the measured
+    # per-SM rates, as a fraction of its duration.
     sm_count = props.multi_processor_count
     clk_sum = clk.summary()
     f_mhz = clk_sum["sm_mhz"] or sm_max_nominal
-    fma_peak = sm_count * 128 * f_mhz * 1e6 / 1e12
-    if not tc_dom:
-        roofline["alu_view"] = {"fma_tflops_achieved": round(Mdom * H["N"] * H["K"] / (us_dom * 1e-6) / 1e12, 3),
-                                "fma_tflops_peak": round(fma_peak, 2), "unit": "T FMA/s",
-                                "frac": round(Mdom * H["N"] * H["K"] / (us_dom * 1e-6) / 1e12 / fma_peak, 4),
-                                "peak_from": f"{sm_count} SMs x 128 FP32 lanes x {f_mhz:.0f} MHz"}
+    bf16_tflops = peak_bf16()
+    roofline["compute_view"] = compute_view(H["fmt"], tc_dom, H["N"], H["K"], Mdom, us_dom, sm_count, f_mhz,
+                                            bf16_tflops)
 
     # End-to-end through the C ABI with host buffers (pinned): per step copy
     # the three activation blocks in, compute, copy the three outputs back.
@@ -424,10 +484,13 @@ def gpu_arm(args, rank, world, local_rank):
         "dtype": "f32", "data": "synthetic (seeded; A ~ N(0,1) bf16, ternary codes U{0,1,2}, d U[0.01,0.05] fp16)",
         "config": {"workload": WORKLOAD,
                    "paths": {str(M): Q2_PATH[H["tc"][M]] for M in H["Ms"]},
-                   "timing": f"CUDA graph of {G} steps replayed {args.steps // G} times",
+                   "timing": f"median of {args.reps} timed regions of {args.steps} steps (each a CUDA graph of "
+                             f"{G} steps replayed {args.steps // G} times, synchronised on both sides)",
                    "weight_bytes_per_call": w.wb, "weight_buffers_cycled": w.nbuf,
                    "l2": f"inputs larger than L2: {w.nbuf} weight buffers = {w.nbuf * w.wb / 2**20:.0f} MiB > 3x L2 ({l2 / 2**20:.0f} MiB)",
                    "pdl": bool(args.pdl), "parallelism": f"replicas x{world}"},
+        "timed_regions_ms": {"median": round(statistics.median(reps_ms), 4), "min": round(min(reps_ms), 4),
+                             "max": round(max(reps_ms), 4), "n": len(reps_ms)},
         "us_per_call": {str(M): round(avg[M], 3) for M in H["Ms"]},
         "pct_of_peak": round(100 * value / world / peak, 2),
         "roofline": roofline, "e2e": e2e,
@@ -437,7 +500,7 @@ def gpu_arm(args, rank, world, local_rank):
     w.free()
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_sweep:
-        line["sweep"] = sweep(l2, peak)
+        line["sweep"] = sweep(l2, peak, sm_count, f_mhz, bf16_tflops)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
     return line
@@ -447,7 +510,10 @@ def e2e_arm(w, H, steps):
     """The same step end to end through the public API with host buffers:
     every step copies the three activation blocks in from pinned host memory
     (one copy: they sit in one pinned buffer), runs the three calls on views
-    of one device buffer, and reads the three outputs back (one copy)."""
+    of one device buffer, and reads the three outputs back (one copy).
+    Timed two ways: the step's API calls captured once into a CUDA graph and
+    replayed per step (copies included in every replay), and the same calls
+    issued from Python every step."""
     import torch
 
     Ms = H["Ms"]
@@ -475,22 +541,49 @@ def e2e_arm(w, H, steps):
             w.call(M, A=vA[M], C=vC[M], tc=H["tc"][M])
         hC.copy_(dC, non_blocking=True)
 
+    def timed(run, n):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run(n)
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1), time.perf_counter() - t0
+
     for _ in range(5):
         step()
+    ms_eager, wall_eager = timed(lambda n: [step() for _ in range(n)], steps)
+    # Graph of G steps (each with its two copies), replayed.
+    G = 50
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            step()
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
-    e1.synchronize()
-    ms = e0.elapsed_time(e1)
-    wall = time.perf_counter() - t0
-    return {"value": w.wb * len(Ms) * steps / (ms * 1e-3) / 1e9, "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "copies_per_step": {"h2d": 1, "d2h": 1}, "wall_s": round(wall, 4)}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(G):
+            step()
+    g.replay()
+    reps = max(1, steps // G)
+
+    def replay(_n):
+        for _ in range(reps):
+            g.replay()
+
+    ms_graph, wall_graph = timed(replay, reps)
+    del g
+    bytes_step = w.wb * len(Ms)
+    return {"value": bytes_step * reps * G / (ms_graph * 1e-3) / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": reps * G,
+            "copies_per_step": {"h2d": 1, "d2h": 1},
+            "how": "the step's public-API calls (H2D copy, three GEMM calls, D2H copy) captured in a CUDA graph of "
+                   f"{G} steps and replayed; every step's copies run inside the timed region",
+            "wall_s": round(wall_graph, 4),
+            "eager": {"value": round(bytes_step * steps / (ms_eager * 1e-3) / 1e9, 2), "unit": UNIT, "steps": steps,
+                      "how": "the same calls issued from Python every step", "wall_s": round(wall_eager, 4)}}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -616,6 +709,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reps", type=int, default=7, help="timed regions of --steps steps; the median is reported")
     ap.add_argument("--case", default=None,
                     help="profiling mode: run --launches calls of one shape, fmt:M:N:K[:tc|:mma] "
                          "(fmt q2|w4|w8), weights cycled past L2; prints one status line")
