@@ -76,9 +76,13 @@ struct Cfg {
   static constexpr int kBody = SW * kStageBytes > kCompute * kSlot ? SW * kStageBytes : kCompute * kSlot;
   // Multi-stage CTAs: the next stage's activations of each warp's block,
   // copied ahead with cp.async ([warp][MT][4 chunks][32 lanes][16 bytes]).
+  // Single-stage CTAs: the stage's activation rows (1024 K each), copied in
+  // bulk by the TMA warp when M > 4, one row per 2064 bytes (the 16-byte pad
+  // spreads the rows over the shared-memory banks).
   static constexpr int kActOff = kBody;
   static constexpr int kActWarp = MT * 4 * 32 * 16;
-  static constexpr int kActBytes = kMulti ? kCompute * kActWarp : 0;
+  static constexpr int kActPitch = kBlocks * 128 * 2 + 16;
+  static constexpr int kActBytes = kMulti ? kCompute * kActWarp : 8 * MT * kActPitch;
   static constexpr int kRecvOff = kActOff + kActBytes;            // ranks 1.. of the cluster, at rank 0
   // Dynamic shared memory for a cluster of `splits` CTAs.
   static constexpr int bytes(int splits) { return kRecvOff + (splits - 1) * kSlot; }
@@ -182,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, kOcc)
   using L = Cfg<MT, kMulti>;
   constexpr int SW = L::SW;
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[2 * SW + 1];   // full[SW], empty[SW], partial sums received
+  // full[SW], empty[SW], partial sums received, activation rows landed
+  __shared__ __align__(8) uint64_t bars[2 * SW + 2];
   __shared__ int abort_sh;
   volatile int* abort_flag = &abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -193,6 +198,11 @@ __global__ void __launch_bounds__(kThreads, kOcc)
   const int st0 = (rank * p.stages) / splits;
   const int T = kMulti ? ((rank + 1) * p.stages) / splits - st0 : 1;   // >= 1: splits <= stages
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[SW]), recv_bar = smem_u32(&bars[2 * SW]);
+  const uint32_t act_bar = recv_bar + 8;
+  // Single-stage CTA with more than 4 rows: the TMA warp copies the stage's
+  // activation rows in bulk (fewer, larger L2 requests than 32 lanes each
+  // loading their 64 bytes).
+  const bool bulk_act = !kMulti && p.M > 4;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SW; ++i) {
@@ -200,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, kOcc)
       mbar_init(empty0 + 8 * i, kCompute);
     }
     mbar_init(recv_bar, 1);
+    mbar_init(act_bar, 1);
     mbar_fence_init();
     if (rank == 0 && splits > 1) mbar_arrive_expect_tx(recv_bar, (splits - 1) * L::kSlot);
     abort_sh = 0;
@@ -224,9 +235,19 @@ __global__ void __launch_bounds__(kThreads, kOcc)
                              n0, full0 + 8 * s, pol);
         issued = t + 1;
       }
+      if (bulk_act) {
+        pdl_wait();                               // activations may belong to the previous grid
+        const int rows = min(p.M, 8 * MT);
+        mbar_arrive_expect_tx(act_bar, rows * (kBlocks * 128 * 2));
+        for (int m = 0; m < rows; ++m)
+          bulk_g2s(smem_u32(smem + L::kActOff + m * L::kActPitch),
+                   p.A + static_cast<size_t>(m) * p.lda + static_cast<size_t>(st0) * kBlocks * 128,
+                   kBlocks * 128 * 2, act_bar);
+      }
       // The CTA may not exit with a copy into its shared memory in flight:
       // stay until the last copies issued have landed.
       for (int t = max(0, issued - SW); t < issued; ++t) mbar_wait(full0 + 8 * (t % SW), (t / SW) & 1, p.err);
+      if (bulk_act) mbar_wait(act_bar, 0, p.err);
     }
     __syncwarp();
     if (splits > 1) cluster_wait();
@@ -264,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, kOcc)
         if constexpr (kMulti) {
           if (g + 8 * mt < p.M) cp_async16(abuf + (mt * 4 + q) * 32 + lane, act_src(t, mt, q));
         } else {
-          act[mt][q] = ld_nc_v4(act_src(t, mt, q));
+          if (!bulk_act) act[mt][q] = ld_nc_v4(act_src(t, mt, q));
         }
       }
     if constexpr (kMulti) cp_async_commit();
@@ -304,6 +325,16 @@ __global__ void __launch_bounds__(kThreads, kOcc)
             r[4 * q + 3] = v.w;
           }
         } else {
+          if (bulk_act) {
+            if (mt == 0) {
+              if (live) live = tc::wait_or_abort(act_bar, 0, p.err, abort_flag);
+              live = __all_sync(0xFFFFFFFFu, live);
+            }
+            const int m = min(g + 8 * mt, p.M - 1);
+            const uint8_t* src = smem + L::kActOff + m * L::kActPitch + (b * 128 + 32 * t4) * 2;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) act[mt][q] = *reinterpret_cast<const uint4*>(src + 16 * q);
+          }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             r[4 * q] = act[mt][q].x;
