@@ -50,10 +50,13 @@
 #include "common.cuh"
 #include "decode.cuh"
 #include "internal.h"
+#include "mma_f16.cuh"
 #include "tc.cuh"
 
 namespace wqp {
 namespace mmaf {
+
+using namespace f16op;
 
 constexpr int kCompute = 8;                  // compute warps: one per 128-K block of a stage
 constexpr int kProducer = kCompute;
@@ -104,94 +107,6 @@ struct Params {
   int red_off, recv_off, bf_off, fo_off;   // shared-memory offsets (ring at 0)
   unsigned* err;
 };
-
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// First MMA of a chain: d = A * B (zero accumulator).
-__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                                uint32_t b0, uint32_t b1) {
-  const float z = 0.f;
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%10,%10,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
-}
-// (hi, lo) floats -> f16x2 (round to nearest even; exact for the scaled
-// activations of at least 2^-17).
-__device__ __forceinline__ uint32_t f32x2_to_f16x2(float hi, float lo) {
-  uint32_t d;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-// Byte i (0..3) of x as two E2M1 codes -> f16x2 (low nibble = first element).
-template <int I>
-__device__ __forceinline__ uint32_t e2m1x2_byte(uint32_t x) {
-  uint32_t d;
-  if constexpr (I == 0)
-    asm("{\n\t.reg .b8 b;\n\tmov.b32 {b, _, _, _}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(d) : "r"(x));
-  else if constexpr (I == 1)
-    asm("{\n\t.reg .b8 b;\n\tmov.b32 {_, b, _, _}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(d) : "r"(x));
-  else if constexpr (I == 2)
-    asm("{\n\t.reg .b8 b;\n\tmov.b32 {_, _, b, _}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(d) : "r"(x));
-  else
-    asm("{\n\t.reg .b8 b;\n\tmov.b32 {_, _, _, b}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(d) : "r"(x));
-  return d;
-}
-// Half h (0: low, 1: high) of x as two E4M3 codes -> f16x2 (low byte first).
-template <int H>
-__device__ __forceinline__ uint32_t e4m3x2_half(uint32_t x) {
-  uint32_t d;
-  if constexpr (H == 0)
-    asm("{\n\t.reg .b16 h;\n\tmov.b32 {h, _}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(d) : "r"(x));
-  else
-    asm("{\n\t.reg .b16 h;\n\tmov.b32 {_, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(d) : "r"(x));
-  return d;
-}
-__device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
-
-// B fragments of one block for one column tile: the 32 activations of row
-// min(g + 8 mt, M - 1) at k = kb + 32 t .. + 31, scaled by 2^e and rounded to
-// FP16 (pairs in k order), and 2^-e, where 2^e puts the block row's largest
-// magnitude in [2^14, 2^15).
-__device__ __forceinline__ void build_bfrag(const Params& p, int kb, int mt, int g, int t4, uint32_t (&bf)[16],
-                                            float& inv) {
-  const int m = min(g + 8 * mt, p.M - 1);         // rows past M: any valid row, results unused
-  const uint16_t* src = p.A + static_cast<size_t>(m) * p.lda + kb + 32 * t4;
-  uint32_t r[16];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = ld_nc_v4(src + 8 * q);
-    r[4 * q] = v.x;
-    r[4 * q + 1] = v.y;
-    r[4 * q + 2] = v.z;
-    r[4 * q + 3] = v.w;
-  }
-  // Largest magnitude of the block row: BF16 magnitudes order like their bits.
-  uint32_t mx = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) mx = __vmaxu2(mx, r[i] & 0x7FFF7FFFu);
-  mx = max(mx & 0xFFFFu, mx >> 16);
-  mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-  mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));   // the 4 lanes of row g hold its 128 activations
-  const int E = static_cast<int>(mx >> 7);              // BF16 exponent field of the maximum
-  const int sh = min(100, max(-113, 141 - E));           // 2^(E - 127 + sh) = 2^14
-  const float scale = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
-  inv = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) bf[i] = f32x2_to_f16x2(bf16hi(r[i]) * scale, bf16lo(r[i]) * scale);
-}
 
 // MT: column tiles of 8 activation rows (1: M <= 8, 2: M <= 16).
 // kRegB: every rank owns one stage, so the B fragments stay in registers.
@@ -348,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, kOcc)
     float2* fos = reinterpret_cast<float2*>(smem + p.fo_off);
     auto build = [&](int kb, int mt, uint32_t (&frag)[16], float (&f)[2]) {
       float inv;
-      build_bfrag(p, kb, mt, g, t4, frag, inv);
+      build_bfrag(p.A, p.lda, p.M, kb, mt, g, t4, frag, inv);
       // This thread's sums are activation rows 2t and 2t + 1 (+ 8 mt): take
       // their 2^-e from lanes 8t and 8t + 4.
       f[0] = __shfl_sync(0xFFFFFFFFu, inv, 8 * t4);
@@ -783,6 +698,19 @@ cudaError_t launch_w8a16_gemm_mma(const GemvArgs& a, cudaStream_t s) {
 // Requires K % 1024 == 0 (checked by the caller).
 cudaError_t launch_w4a16_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   using namespace mmaf;
+  // Fewer than two 64-row tiles per SM (and at most 8 stages): short CTAs,
+  // three per SM, 8 rows per launch. The choice depends on the shape only,
+  // so a row's result does not depend on M.
+  if (w4a16_short_fits(a)) {
+    if (a.M <= 8) return launch_w4a16_gemm_short(a, s);
+    GemvArgs lo = a, hi = a;
+    lo.M = 8;
+    hi.M = a.M - 8;
+    hi.A = static_cast<const uint16_t*>(a.A) + static_cast<size_t>(8) * a.lda;
+    hi.C = static_cast<uint16_t*>(a.C) + static_cast<size_t>(8) * a.ldc;
+    const cudaError_t e1 = launch_w4a16_gemm_short(lo, s);
+    return e1 != cudaSuccess ? e1 : launch_w4a16_gemm_short(hi, s);
+  }
   const uint64_t K = static_cast<uint64_t>(a.K);
   CUtensorMap mw, ms;
   cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, K / 2, static_cast<uint64_t>(a.N), K / 2, 64,

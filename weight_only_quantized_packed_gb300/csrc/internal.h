@@ -72,6 +72,10 @@ cudaError_t launch_q2_gemm_stream(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_w4a16_gemm_tc(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_w8a16_gemm_mma(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_w4a16_gemm_mma(const GemvArgs& a, cudaStream_t s);
+// W4 short-CTA kernel (gemm_mma_w4s.cu): shapes it serves, and its launch
+// (M <= 8 per launch).
+bool w4a16_short_fits(const GemvArgs& a);
+cudaError_t launch_w4a16_gemm_short(const GemvArgs& a, cudaStream_t s);
 
 cudaError_t launch_q2_dequant(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_w4a16_dequant(const DequantArgs& a, cudaStream_t s);
