@@ -45,7 +45,8 @@ KERNEL_SOURCES = {False: ["gemv_scalar.cuh", "gemv_q2.cu", "decode.cuh", "common
                   True: ["gemm_tc.cu", "tc.cuh", "decode.cuh", "common.cuh"],
                   "mma": ["gemm_mma.cu", "tc.cuh", "common.cuh"],
                   "stream": ["gemm_mma_stream.cu", "tc.cuh", "common.cuh"],
-                  "f16": ["gemm_mma_f16.cu", "tc.cuh", "decode.cuh", "common.cuh"]}
+                  "f16": ["gemm_mma_f16.cu", "mma_f16.cuh", "tc.cuh", "decode.cuh", "common.cuh"],
+                  "w4s": ["gemm_mma_w4s.cu", "mma_f16.cuh", "tc.cuh", "decode.cuh", "common.cuh"]}
 # Q2_0 entry point per path key (False: scalar, True: tcgen05, "mma": mma.sync).
 Q2_PATH = {False: "q2_gemv", True: "q2_gemm_tc", "mma": "q2_gemm_mma"}
 

@@ -66,8 +66,8 @@ constexpr int kBlocks = 8;                   // 128-K blocks per stage (1024 K)
 constexpr int kMaxSplits = 8;
 constexpr int kMaxRing = 8;
 
-// FP8 stage: 8 boxes of 32 rows x 128 bytes (128-byte swizzle), then the 8
-// FP32 block scales of the tile's 128-row group. Tiles of 32 rows keep a
+// FP8 stage: 8 blocks of 32 rows x 128 bytes (128-byte swizzle; one 3-D
+// copy), then the 8 FP32 block scales of the tile's 128-row group. Tiles of 32 rows keep a
 // stage at 33 KB, so six stages stay in flight per SM.
 struct Fp8F {
   static constexpr bool kW4 = false;
@@ -78,8 +78,8 @@ struct Fp8F {
   static constexpr int kTxBytes = kScaleOff + kBlocks * 4;
   static constexpr int kStageBytes = kScaleOff + 1024;                  // keeps slots 1024-aligned
 };
-// W4 stage: 8 boxes of 64 rows x 64 bytes of codes, then 64 rows x 64 bytes
-// of E4M3 group scales (8 blocks x 8 groups of 16 K).
+// W4 stage: 8 blocks of 64 rows x 64 bytes of codes (one 3-D copy), then
+// 64 rows x 64 bytes of E4M3 group scales (8 blocks x 8 groups of 16 K).
 struct W4F {
   static constexpr bool kW4 = true;
   static constexpr int BM = 64;
@@ -164,10 +164,9 @@ __global__ void __launch_bounds__(kThreads, kOcc)
         const int tile = cl + (it / nst) * C, st = st0 + it % nst;
         const uint32_t dst = smem_u32(smem + s * F::kStageBytes), bar = full0 + 8 * s;
         mbar_arrive_expect_tx(bar, F::kTxBytes);
-#pragma unroll 1
-        for (int b = 0; b < kBlocks; ++b)
-          tc::tma_load_2d_hint(dst + b * F::kBoxBytes, &tmW, (st * kBlocks + b) * (F::kW4 ? 64 : 128), tile * BM, bar,
-                               pol);
+        // One copy of the stage's 8 blocks (a 3-D view: bytes of a block's
+        // row, rows, blocks), landing block after block.
+        tc::tma_load_3d_hint(dst, &tmW, 0, tile * BM, st * kBlocks, bar, pol);
         if constexpr (F::kW4)
           tc::tma_load_2d_hint(dst + F::kScaleOff, &tmS, st * 64, tile * BM, bar, pol);
         else
@@ -685,8 +684,9 @@ cudaError_t launch_w8a16_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   using namespace mmaf;
   const uint64_t K = static_cast<uint64_t>(a.K);
   CUtensorMap mw, ms;
-  cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, K, static_cast<uint64_t>(a.N), K, 128,
-                                Fp8F::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  // Codes as [K/128 blocks][N rows][128 bytes]: row pitch K, block pitch 128.
+  cudaError_t e = cached_map_3d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, {128, static_cast<uint64_t>(a.N), K / 128},
+                                {K, 128}, {128, Fp8F::BM, kBlocks}, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   // Block scales [ceil(N/128), K/128] FP32: one box of the stage's 8 scales.
   e = cached_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.scales, K / 128, static_cast<uint64_t>((a.N + 127) / 128),
@@ -713,8 +713,9 @@ cudaError_t launch_w4a16_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   }
   const uint64_t K = static_cast<uint64_t>(a.K);
   CUtensorMap mw, ms;
-  cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, K / 2, static_cast<uint64_t>(a.N), K / 2, 64,
-                                W4F::BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+  // Codes as [K/128 blocks][N rows][64 bytes]: row pitch K/2, block pitch 64.
+  cudaError_t e = cached_map_3d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, {64, static_cast<uint64_t>(a.N), K / 128},
+                                {K / 2, 64}, {64, W4F::BM, kBlocks}, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   e = cached_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, K / 16, static_cast<uint64_t>(a.N), K / 16, 64,
                     W4F::BM, CU_TENSOR_MAP_SWIZZLE_NONE);

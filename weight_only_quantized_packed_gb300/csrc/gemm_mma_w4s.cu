@@ -11,9 +11,9 @@
 // (activation row, 128-K block) by a power of two and rounded to FP16, and
 // each block's FP32 sum is multiplied back by 2^-e once.
 //
-// CTA: 64 weight rows x one stage (8 blocks of 128 K: 8 boxes of 64 rows x
-// 64 bytes of codes and one box of 64 rows x 64 bytes of E4M3 scales, by
-// TMA); 8 compute warps (warp w owns block w for all four 16-row tiles) and
+// CTA: 64 weight rows x one stage (8 blocks of 128 K: one 3-D copy of 8
+// blocks x 64 rows x 64 bytes of codes and one box of 64 rows x 64 bytes of
+// E4M3 scales, by TMA); 8 compute warps (warp w owns block w for all four 16-row tiles) and
 // one TMA warp. A cluster of one CTA per stage splits K; ranks >= 1 send their
 // sums to rank 0 with st.async and leave at once (their SM slots go to the
 // next call's CTAs), rank 0 adds them in rank order and stores. With more
@@ -94,8 +94,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       tc::prefetch_tmap(&tmS);
       const uint64_t pol = policy_evict_first();
       mbar_arrive_expect_tx(full, kStageBytes);
-      for (int b = 0; b < kBlocks; ++b)
-        tc::tma_load_2d_hint(smem_u32(smem + b * kBoxBytes), &tmW, (rank * kBlocks + b) * 64, n0, full, pol);
+      tc::tma_load_3d_hint(smem_u32(smem), &tmW, 0, n0, rank * kBlocks, full, pol);   // the stage's 8 blocks
       tc::tma_load_2d_hint(smem_u32(smem + kScaleOff), &tmS, rank * 64, n0, full, pol);
       if (bulk_act) {
         pdl_wait();                               // activations may belong to the previous grid
@@ -281,8 +280,9 @@ cudaError_t launch_w4a16_gemm_short(const GemvArgs& a, cudaStream_t s) {
   using namespace mmaw4s;
   const uint64_t K = static_cast<uint64_t>(a.K);
   CUtensorMap mw, ms;
-  cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, K / 2, static_cast<uint64_t>(a.N), K / 2, 64,
-                                BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+  // Codes as [K/128 blocks][N rows][64 bytes]: row pitch K/2, block pitch 64.
+  cudaError_t e = cached_map_3d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, {64, static_cast<uint64_t>(a.N), K / 128},
+                                {K / 2, 64}, {64, BM, kBlocks}, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
   e = cached_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, K / 16, static_cast<uint64_t>(a.N), K / 16, 64, BM,
                     CU_TENSOR_MAP_SWIZZLE_NONE);

@@ -93,6 +93,14 @@ cudaError_t cached_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ba
                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                           CUtensorMapSwizzle sw);
 
+// 3-D tensor map (tmap.cu): dims innermost first, byte strides of dims 1 and
+// 2 (any order in memory: a block-of-rows view uses a row pitch for dim 1
+// and a smaller block pitch for dim 2), box per dim; and its cached form.
+cudaError_t make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t (&dims)[3],
+                        const uint64_t (&strides_bytes)[2], const uint32_t (&box)[3], CUtensorMapSwizzle sw);
+cudaError_t cached_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t (&dims)[3],
+                          const uint64_t (&strides_bytes)[2], const uint32_t (&box)[3], CUtensorMapSwizzle sw);
+
 // Launch helper: programmatic stream serialization when pdl is set.
 template <typename Kern, typename... Args>
 cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
