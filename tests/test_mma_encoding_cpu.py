@@ -8,7 +8,11 @@ The emulation follows the kernel's data flow lane by lane:
     them in place: (w & 0x00030003 << 2x) and ((w >> 8) & ...);
   * it pairs its 32 activations (k = 32 t .. 32 t + 31 of row g) with byte
     permutes and multiplies them by 2^(64 - 2x);
-  * the chain starts from an MMA with every code 1, negated;
+  * the chain starts from the block's offset -2^-69 * sum_k a: four MMAs with
+    the lane's raw activations as the A operand (rows g and g + 8 each hold
+    half of activation row g) against -2^-69 in every B element, the two
+    halves added, and the sums of activation rows 2t and 2t + 1 taken from
+    lanes 8t and 8t + 4 (the shuffle) as the chain's C input;
 and places every register into the m16n8k16 matrices by the fragment layout
 the PTX ISA gives for .bf16 operands. The products are exact, so the float64
 sums must equal the formula bit for bit: a wrong lane assignment, permute
@@ -67,7 +71,11 @@ def mma_fragments_to_matrices(a_regs, b_regs):
     return A, B
 
 
-def emulate_block(codes, act_bits, scale_exp=lambda x: 64 - 2 * x, swap_a_halves=False, offset=True):
+NEG_UNIT = 0x9D009D00      # -2^-69 in both BF16 halves
+
+
+def emulate_block(codes, act_bits, scale_exp=lambda x: 64 - 2 * x, swap_a_halves=False, offset=True,
+                  offset_src=lambda t: (8 * t, 8 * t + 4)):
     """One warp, one block, one row tile: D[row, m] = 2^-69 sum_k (c - 1) a.
     The keyword arguments plant mistakes for the tests that must catch them."""
     # Code words: word i of row r holds codes 16 i .. 16 i + 15, code q at bits 2q.
@@ -76,8 +84,7 @@ def emulate_block(codes, act_bits, scale_exp=lambda x: 64 - 2 * x, swap_a_halves
         words |= codes[:, q::16].astype(np.uint64) << np.uint64(2 * q)
     words = words.astype(np.uint32)
     D = np.zeros((16, 8))
-    neg_ones = [0x80008000 | (0x00010001 << (2 * x)) for x in range(4)]
-    # B fragments and the offset chain (built once per block).
+    # B fragments (built once per block).
     bregs = []
     for st in range(8):
         x, o = st & 3, 8 * (st >> 2) + ((st & 3) >> 1)
@@ -90,9 +97,26 @@ def emulate_block(codes, act_bits, scale_exp=lambda x: 64 - 2 * x, swap_a_halves
             b1 = mul_pow2_bf16x2(byte_perm(r[o + 2], r[o + 6], sel), scale_exp(x))
             per_lane.append((b0, b1))
         bregs.append(per_lane)
-    for st in range(8 if offset else 0):
-        A, B = mma_fragments_to_matrices([[neg_ones[st & 3]] * 4 for _ in range(32)], bregs[st])
-        D += A @ B
+    if offset:
+        # Four MMAs: lane (g, t) passes its raw activation registers 4j .. 4j + 3.
+        O = np.zeros((16, 8))
+        for j in range(4):
+            a_regs = []
+            for lane in range(32):
+                g, t = lane // 4, lane % 4
+                r = [int(act_bits[g, 32 * t + 2 * i]) | (int(act_bits[g, 32 * t + 2 * i + 1]) << 16) for i in range(16)]
+                a_regs.append(r[4 * j:4 * j + 4])
+            A, B = mma_fragments_to_matrices(a_regs, [[NEG_UNIT, NEG_UNIT]] * 32)
+            O += A @ B
+        # Lane (g, t) holds D[g, 2t] and D[g + 8, 2t]; their sum is its s.
+        s = [O[lane // 4, 2 * (lane % 4)] + O[lane // 4 + 8, 2 * (lane % 4)] for lane in range(32)]
+        # The chain's C input of lane (g, t): columns 2t and 2t + 1 of rows g and g + 8.
+        for lane in range(32):
+            g, t = lane // 4, lane % 4
+            src0, src1 = offset_src(t)
+            for row in (g, g + 8):
+                D[row, 2 * t] += s[src0]
+                D[row, 2 * t + 1] += s[src1]
     # The codes' chain.
     for st in range(8):
         m = 0x00030003 << (2 * (st & 3))
@@ -149,7 +173,8 @@ def test_a_wrong_permute_is_caught():
 @pytest.mark.parametrize("mistake", [
     dict(scale_exp=lambda x: 64 - x),        # pre-scale exponent per position off
     dict(swap_a_halves=True),                # codes (x, 8+x) and (4+x, 12+x) swapped
-    dict(offset=False),                      # the "- 1" (negated code-1 chain) dropped
+    dict(offset=False),                      # the "- 1" (the offset) dropped
+    dict(offset_src=lambda t: (4 * t, 4 * t + 1)),   # offsets fetched from the wrong lanes
 ])
 def test_planted_mistakes_are_caught(mistake):
     rng = np.random.default_rng(13)

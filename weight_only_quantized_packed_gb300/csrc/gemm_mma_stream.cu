@@ -45,9 +45,9 @@
 //     past M repeat row M - 1): the 32 activations of k = 128 b + 32 t .. + 31,
 //     paired the same way and multiplied by 2^(64 - 2x), so every product is
 //     c * a * 2^-69 exactly.
-//   * Each tile's chain starts from -2^-69 * sum_k a (an MMA chain with every
-//     code 1 and a negative sign, run once per block and call), so it ends at
-//     2^-69 * sum_k (c - 1) a.
+//   * Each tile's chain starts from -2^-69 * sum_k a (four MMAs per block
+//     with the raw activations as the A operand and -2^-69 as B, run once per
+//     block and call), so it ends at 2^-69 * sum_k (c - 1) a.
 //   * acc += d * chain, and C = bf16(acc * 2^69).
 // Every wait is bounded (2 s of wall time); on expiry the CTA records the
 // device error, skips the rest of its work, and still reaches the final
@@ -151,14 +151,30 @@ __device__ __forceinline__ float load_d(const uint8_t* blk) {
   return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk + 32)));
 }
 
-// -(4^x) * 2^-133 in both BF16 lanes: the "code 1, negated" operand.
-__device__ __forceinline__ constexpr uint32_t neg_ones(int x) { return 0x80008000u | (0x00010001u << (2 * x)); }
+// -2^-69 in both BF16 lanes.
+constexpr uint32_t kNegUnit = 0x9D009D00u;
 // 2^(64 - 2x) in both BF16 lanes.
 __device__ __forceinline__ constexpr uint32_t prescale(int x) { return ((191u - 2u * x) << 7) * 0x00010001u; }
 
+// The offset -2^-69 * sum_k a of a block for the activation rows of this
+// thread's MMA columns 2t and 2t + 1. Four MMAs take the thread's 32 raw
+// activations (row g) as the A operand, so rows g and g + 8 of the MMA each
+// sum half of activation row g, against -2^-69 in every B element (every
+// product exact); the two halves are added and each column's row sum is
+// fetched from a lane of group 2t or 2t + 1.
+__device__ __forceinline__ void offset_sums(const uint32_t (&r)[16], int t4, float (&ns)[2]) {
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) mma_bf16_16816(o, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3], kNegUnit, kNegUnit);
+  const float s = o[0] + o[2];
+  ns[0] = __shfl_sync(0xFFFFFFFFu, s, 8 * t4);
+  ns[1] = __shfl_sync(0xFFFFFFFFu, s, 8 * t4 + 4);
+}
+
 // B fragments of one block for one column tile: this thread's 32 activations
 // (row min(g + 8 mt, M - 1), k = kb + 32 t .. + 31) permuted to the code-pair
-// order and pre-scaled, and the offset chain -2^-69 * sum_k a of its row.
+// order and pre-scaled, and the offset -2^-69 * sum_k a of the activation rows
+// of its MMA columns.
 __device__ __forceinline__ void build_bfrag(const StreamParams& p, int kb, int mt, int g, int t4, uint32_t (&bf)[16],
                                             float (&ns)[2]) {
   const int m = min(g + 8 * mt, p.M - 1);         // rows past M: any valid row, results unused
@@ -179,14 +195,7 @@ __device__ __forceinline__ void build_bfrag(const StreamParams& p, int kb, int m
     bf[2 * st] = mul_bf16x2(__byte_perm(r[o], r[o + 4], sel), prescale(x));
     bf[2 * st + 1] = mul_bf16x2(__byte_perm(r[o + 2], r[o + 6], sel), prescale(x));
   }
-  float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int st = 0; st < 8; ++st) {
-    const uint32_t no = neg_ones(st & 3);
-    mma_bf16_16816(c, no, no, no, no, bf[2 * st], bf[2 * st + 1]);
-  }
-  ns[0] = c[0];   // rows g and g + 8 of the all-ones operand give the same sums
-  ns[1] = c[1];
+  offset_sums(r, t4, ns);
 }
 
 // MT: column tiles of 8 activation rows (1: M <= 8, 2: M <= 16).
