@@ -118,6 +118,20 @@ def test_q2_code3_and_closed_form(oracle_lib):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+def test_activation_range(oracle_lib, fmt):
+    """Activations scaled by 2^40 and 2^-40: within the Q2_0 kernel's stated
+    range (pre-scaled activations finite for |a| < 2^48, products normal for
+    |a| >= 2^-57); the other formats take any finite activation."""
+    for scale in (2.0 ** 40, 2.0 ** -40):
+        M, N, K = 4, 300, 2048
+        d = G.make(fmt, M, N, K, seed=91)
+        d["A"] = synth.activations(M, K, 92, scale=scale)
+        d["dA"] = G.dev_bf16(d["A"])
+        C = G.host_bits(G.run_gpu(d))
+        assert_scalar_term(C, G.run_oracle(oracle_lib, d), K, f"{fmt} activation scale {scale:g}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 def test_strided_rows_and_canary(oracle_lib, fmt):
     """Row pitches lda > K and ldc > N; bytes outside C's rows stay untouched."""
     M, N, K = 6, 70, 1024

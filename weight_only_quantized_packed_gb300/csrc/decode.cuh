@@ -1,7 +1,8 @@
 // In-register decoders for the three packed weight formats. Every decoded
 // weight is exact (every Q2_0, E2M1 and E4M3 value is a BF16 and an FP32
-// value). The dequant kernels use the same FP32 decoders as the scalar
-// GEMVs, so the bit-exact dequant tests cover the GEMV decode path too.
+// value; the Q2_0 FP32 decode carries a power-of-two position factor). The
+// dequant kernels use the same FP32 decoders as the scalar GEMVs, so the
+// bit-exact dequant tests cover the GEMV decode path too.
 #pragma once
 #include <cuda_fp16.h>
 
@@ -38,29 +39,28 @@ __device__ __forceinline__ void q2_decode_word(uint32_t q, uint32_t (&p)[8]) {
   p[7] = sub_bf16x2((q12 & 0x000C000Cu) | 0x42004200u, 0x42044204u);
 }
 
-// FP32 decode of a 16-code word q (code j at bits 2j). For j <= 10 the field
-// is OR-ed, in place, into the mantissa of 2^23: v = 2^23 + c * 4^j exactly,
-// and v - (2^23 + 4^j) = (c - 1) * 4^j. Codes 11..15 are shifted down by 22
-// bits first, so their weights are 4^(j-11). w[i] = (w_{2i}, w_{2i+1}) holds
-// (c_j - 1) * q2_pos_weight(j); a consumer multiplies by the activation
-// pre-scaled by 1 / q2_pos_weight(j), a power of two, so every product equals
-// a * (c - 1) exactly.
+// Position factor of code j of a 16-code word: 4^j for j <= 10, 4^(j - 11)
+// for j >= 11 (those fields are shifted down by 22 bits before masking).
 __host__ __device__ constexpr float q2_pos_weight(int p) {
   return p <= 10 ? static_cast<float>(1u << (2 * p)) : static_cast<float>(1u << (2 * (p - 11)));
 }
 
-__device__ __forceinline__ void q2_decode_f32(uint32_t q, float2 (&w)[8]) {
+// FP32 decode of a 16-code word q (code j at bits 2j) with one mask per code:
+// the field of code j, masked in place, read as FP32 bits is the subnormal
+// c_j * q2_pos_weight(j) * 2^-149, exactly. w[i] = (w_{2i}, w_{2i+1}). A
+// consumer multiplies it by the activation pre-scaled by
+// 2^80 / q2_pos_weight(j) (a power of two), so every product is
+// c * a * 2^-69 exactly, and accounts for the -1 of every code by starting
+// each 16-code sum from -2^-69 * sum a.
+__device__ __forceinline__ void q2_decode_sub(uint32_t q, float2 (&w)[8]) {
   const uint32_t q22 = q >> 22;
   float v[16];
 #pragma unroll
-  for (int j = 0; j < 11; ++j) v[j] = __uint_as_float(0x4B000000u | (q & (3u << (2 * j))));
+  for (int j = 0; j < 11; ++j) v[j] = __uint_as_float(q & (3u << (2 * j)));
 #pragma unroll
-  for (int j = 11; j < 16; ++j) v[j] = __uint_as_float(0x4B000000u | (q22 & (3u << (2 * (j - 11)))));
+  for (int j = 11; j < 16; ++j) v[j] = __uint_as_float(q22 & (3u << (2 * (j - 11))));
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    w[i] = __fadd2_rn(make_float2(v[2 * i], v[2 * i + 1]),
-                      make_float2(-(8388608.0f + q2_pos_weight(2 * i)),
-                                  -(8388608.0f + q2_pos_weight(2 * i + 1))));
+  for (int i = 0; i < 8; ++i) w[i] = make_float2(v[2 * i], v[2 * i + 1]);
 }
 
 // The 16 codes of word w (0..7) of a block that starts at a 2-byte aligned

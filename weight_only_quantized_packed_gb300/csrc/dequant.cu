@@ -15,14 +15,16 @@ __global__ void q2_dequant_kernel(const uint8_t* W, float* out, int N, int K) {
     const uint8_t* b = W + blk * 34;
     float2 v[8];
     const uint16_t* b16 = reinterpret_cast<const uint16_t*>(b);
-    q2_decode_f32(static_cast<uint32_t>(__ldg(b16 + 2 * w)) | (static_cast<uint32_t>(__ldg(b16 + 2 * w + 1)) << 16), v);
+    q2_decode_sub(static_cast<uint32_t>(__ldg(b16 + 2 * w)) | (static_cast<uint32_t>(__ldg(b16 + 2 * w + 1)) << 16), v);
     const float d = __half2float(__ushort_as_half(__ldg(b16 + 16)));
     float* o = out + (blk / G) * static_cast<long long>(K) + (blk % G) * 128 + 16 * w;
-    // (c - 1) * 4^j * 4^-j is exact; then one multiply by d, as in the oracle.
+    // c * 4^j * 2^-149 times 2^75 and 2^74 / 4^j is the code c, exactly;
+    // then (c - 1) times d, one rounding as in the oracle.
+    constexpr float kTwo75 = 37778931862957161709568.0f, kTwo74 = 18889465931478580854784.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      o[2 * i] = (v[i].x * (1.0f / q2_pos_weight(2 * i))) * d;
-      o[2 * i + 1] = (v[i].y * (1.0f / q2_pos_weight(2 * i + 1))) * d;
+      o[2 * i] = ((v[i].x * kTwo75) * (kTwo74 / q2_pos_weight(2 * i)) - 1.0f) * d;
+      o[2 * i + 1] = ((v[i].y * kTwo75) * (kTwo74 / q2_pos_weight(2 * i + 1)) - 1.0f) * d;
     }
   }
 }

@@ -27,14 +27,31 @@ struct Q2Fmt {
     uint16_t* d = reinterpret_cast<uint16_t*>(dst);
     for (int i = lane; i < 17 * tg; i += 32) d[i] = __ldg(src + i);
   }
-  // The activation at position p of a 16-K segment is pre-scaled by the
-  // inverse of the decoded weight's position factor (see q2_decode_f32).
-  __device__ static constexpr float prescale(int pos) { return 1.0f / q2_pos_weight(pos); }
+  // The activation at position p of a 16-K segment is pre-scaled by
+  // 2^80 over the decoded weight's position factor (see q2_decode_sub), so
+  // each product is c * a * 2^-69; each segment's sum starts from its
+  // offset -2^-69 * sum a (the -1 of every code), and the output is scaled
+  // back by 2^69. The pre-scaled activations stay finite for |a| < 2^48, and
+  // the products stay normal for |a| >= 2^-57.
+  static constexpr bool kOffset = true;
+  static constexpr float kOutScale = 590295810358705651712.0f;   // 2^69
+  __device__ static constexpr float prescale(int pos) {
+    return 1208925819614629174706176.0f / q2_pos_weight(pos);   // 2^80 / factor
+  }
+  // 2^-69 * (sum of the 16 activations in v0, v1), added in a fixed tree.
+  __device__ static float seg_offset(uint4 v0, uint4 v1) {
+    const float2 p0 = __fadd2_rn(make_float2(bf16lo(v0.x), bf16hi(v0.x)), make_float2(bf16lo(v0.y), bf16hi(v0.y)));
+    const float2 p1 = __fadd2_rn(make_float2(bf16lo(v0.z), bf16hi(v0.z)), make_float2(bf16lo(v0.w), bf16hi(v0.w)));
+    const float2 p2 = __fadd2_rn(make_float2(bf16lo(v1.x), bf16hi(v1.x)), make_float2(bf16lo(v1.y), bf16hi(v1.y)));
+    const float2 p3 = __fadd2_rn(make_float2(bf16lo(v1.z), bf16hi(v1.z)), make_float2(bf16lo(v1.w), bf16hi(v1.w)));
+    const float2 q = __fadd2_rn(__fadd2_rn(p0, p1), __fadd2_rn(p2, p3));
+    return (q.x + q.y) * 1.6940658945086007e-21f;                  // 2^-69
+  }
   // Segment sg of a tile = word (sg % 8) of block (sg / 8): K offset 16 * sg.
   __device__ static void decode(const ScalarParams&, int, int, int sg, const uint8_t* sW, const uint8_t*,
                                 Seg& g) {
     const uint8_t* blk = sW + (sg >> 3) * 34;
-    q2_decode_f32(q2_code_word(blk, sg & 7), g.w);
+    q2_decode_sub(q2_code_word(blk, sg & 7), g.w);
     g.s = q2_scale(blk);
   }
 };

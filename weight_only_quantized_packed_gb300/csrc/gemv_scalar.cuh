@@ -22,9 +22,11 @@
 // rows, and the consumers widen them tile by tile behind a named barrier.
 //
 // Per-row arithmetic (identical for every M, so a batched row equals the M = 1
-// row bit for bit): weights are decoded to exact FP32 values. For each
-// 16-weight segment a lane owns, two chains of packed FFMA2 (k = 0..7 and
-// k = 8..15, even and odd k in the two halves) are added, the segment's scale
+// row bit for bit): weights are decoded to exact FP32 values (Q2_0: the code
+// times a power of two, and the chain of each segment starts from the
+// segment's -2^-69 * sum a, computed once when the activations are widened).
+// For each 16-weight segment a lane owns, two chains of packed FFMA2
+// (k = 0..7 and k = 8..15, even and odd k in the two halves) are added, the segment's scale
 // is folded with one FFMA2 onto the lane's accumulator pair, and at the end
 // the pair is summed and the 32 lanes reduced by a fixed xor-butterfly. The
 // order depends only on N and K, never on M or on the staging path.
@@ -90,19 +92,28 @@ __device__ __forceinline__ void widen_segment(uint4 v0, uint4 v1, float* row, in
 //   issue_tile(...)     producer lane: tensor-map copies of one K tile
 //   copy_row_plain(...) producer warp: plain-load copy of one row's tile
 //   prescale(p)         factor applied to a[k] when widened (p = k % 16)
+//   kOffset             each 16-K segment's sum starts from -seg_offset(a)
+//                       (Q2_0: the -1 of every code), stored when widened
+//   kOutScale           factor applied to the FP32 result before the store
 //   decode(...)         consumer: one segment of one row -> Seg
 template <class F, int M, bool ARES>
 struct ScalarCfg {
-  static constexpr int kStages = ARES ? (M <= 2 ? 6 : 4) : ((M <= 4) ? 4 : (M <= 8 ? 3 : 2));
-  static constexpr bool kFADouble = !ARES && (M <= 4);    // double-buffered per-tile FP32 A
   static constexpr int kW2Off = kRows * F::kWRow;
   static constexpr int kWStage = (kRows * (F::kWRow + F::kW2Row) + 127) / 128 * 128;
+  // Ring depth. With resident activations and M >= 3 the ring is kept near
+  // 24 KB, so that two CTAs still fit on an SM beside up to 80 KB of FP32
+  // activations each.
+  static constexpr int kStages = ARES ? (M <= 2 ? 6 : (kWStage > 8192 ? 2 : 4))
+                                      : ((M <= 4) ? 4 : (M <= 8 ? 3 : 2));
+  static constexpr bool kFADouble = !ARES && (M <= 4);    // double-buffered per-tile FP32 A
   static constexpr int kAW = F::kTK < 512 ? F::kTK : 512;   // K per activation box
   static constexpr int kAStage = ARES ? 0 : M * F::kTK * 2;
   static constexpr int kStageBytes = ((kWStage + kAStage) + 127) / 128 * 128;
   static constexpr int kFABytes = ARES ? 0 : M * F::kTK * 4;  // one per-tile FP32 buffer
-  static constexpr int kSmemFixed = kStages * kStageBytes + (kFADouble ? 2 : 1) * kFABytes;
-  static constexpr int kSmemMax = kSmemFixed + (ARES ? kAResMaxBytes : 0);
+  static constexpr int kOffBytes = (ARES || !F::kOffset) ? 0 : M * (F::kTK / 16) * 4;   // its segment offsets
+  static constexpr int kSmemFixed = kStages * kStageBytes + (kFADouble ? 2 : 1) * (kFABytes + kOffBytes);
+  // Resident activations: M * K FP32 values, then M * K / 16 segment offsets.
+  static constexpr int kSmemMax = kSmemFixed + (ARES ? kAResMaxBytes + (F::kOffset ? kAResMaxBytes / 16 : 0) : 0);
   static constexpr int kMinBlocks = (M <= 8) ? 2 : 1;
   static_assert(kSmemMax <= 227 * 1024, "shared memory budget");
   static_assert(F::kW2Row == 0 || (kRows * F::kWRow) % 128 == 0, "second weight block alignment");
@@ -131,6 +142,9 @@ __global__ void __launch_bounds__(kThreads, (ScalarCfg<F, M, ARES>::kMinBlocks))
   const int tiles = (G + kGT - 1) / kGT;
   float* fA = reinterpret_cast<float*>(smem + kStages * Cfg::kStageBytes);
   const int ldfa = ARES ? K : TK;                // FP32 activation row pitch (floats)
+  // Segment offsets (formats with kOffset): after the FP32 activations.
+  float* fOff = fA + (ARES ? M * K : (Cfg::kFADouble ? 2 : 1) * M * TK);
+  const int ldoff = ldfa / 16;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -200,7 +214,9 @@ __global__ void __launch_bounds__(kThreads, (ScalarCfg<F, M, ARES>::kMinBlocks))
       const int m = u / segK;
       const int sg = u - m * segK;
       const uint4* src = reinterpret_cast<const uint4*>(p.A + static_cast<size_t>(m) * p.lda + sg * 16);
-      widen_segment<F>(__ldg(src), __ldg(src + 1), fA + m * ldfa, sg);
+      const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      widen_segment<F>(v0, v1, fA + m * ldfa, sg);
+      if constexpr (F::kOffset) fOff[m * ldoff + sg] = F::seg_offset(v0, v1);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory");
   }
@@ -225,14 +241,18 @@ __global__ void __launch_bounds__(kThreads, (ScalarCfg<F, M, ARES>::kMinBlocks))
     const int segs = tg * 8;
     const uint8_t* sW = smem + s * Cfg::kStageBytes;
     const float* fAt;
+    const float* fOt;
     int sg0;                                      // segment offset of this tile in fAt
     if (ARES) {
       fAt = fA;
+      fOt = fOff;
       sg0 = t * kSegT;
     } else {
       const uint16_t* sAs = reinterpret_cast<const uint16_t*>(sW + Cfg::kWStage);
       float* fAw = fA + (Cfg::kFADouble ? (t & 1) * (M * TK) : 0);
+      float* fOw = fOff + (Cfg::kFADouble ? (t & 1) * (M * kSegT) : 0);
       fAt = fAw;
+      fOt = fOw;
       sg0 = 0;
       // With a single FP32 buffer, wait until every warp is done with the
       // previous tile before overwriting it.
@@ -245,7 +265,9 @@ __global__ void __launch_bounds__(kThreads, (ScalarCfg<F, M, ARES>::kMinBlocks))
           const int k0 = sg * 16;
           const uint4* src = reinterpret_cast<const uint4*>(
               sAs + (k0 / Cfg::kAW) * (M * Cfg::kAW) + m * Cfg::kAW + (k0 % Cfg::kAW));
-          widen_segment<F>(src[0], src[1], fAw + m * ldfa, sg);
+          const uint4 v0 = src[0], v1 = src[1];
+          widen_segment<F>(v0, v1, fAw + m * ldfa, sg);
+          if constexpr (F::kOffset) fOw[m * ldoff + sg] = F::seg_offset(v0, v1);
         }
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory");
@@ -255,14 +277,10 @@ __global__ void __launch_bounds__(kThreads, (ScalarCfg<F, M, ARES>::kMinBlocks))
         Seg g[kRowsPerWarp];
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) {
-          if (r0 + r < rows) {
-            F::decode(p, n0 + r0 + r, t, sg, sW + (r0 + r) * F::kWRow,
-                      sW + Cfg::kW2Off + (r0 + r) * F::kW2Row, g[r]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) g[r].w[i] = make_float2(0.f, 0.f);
-            g[r].s = 0.f;
-          }
+          // A row past N decodes the last valid row instead (no branch; its
+          // sums are never stored).
+          const int rr = min(r0 + r, rows - 1);
+          F::decode(p, n0 + rr, t, sg, sW + rr * F::kWRow, sW + Cfg::kW2Off + rr * F::kW2Row, g[r]);
         }
         const int sa = sg0 + sg;
 #pragma unroll
@@ -274,9 +292,11 @@ __global__ void __launch_bounds__(kThreads, (ScalarCfg<F, M, ARES>::kMinBlocks))
                                make_float2(q1.x, q1.y), make_float2(q1.z, q1.w),
                                make_float2(q2.x, q2.y), make_float2(q2.z, q2.w),
                                make_float2(q3.x, q3.y), make_float2(q3.z, q3.w)};
+          float2 c00 = make_float2(0.f, 0.f);     // where each row's chain starts
+          if constexpr (F::kOffset) c00.x = -fOt[m * ldoff + sa];
 #pragma unroll
           for (int r = 0; r < kRowsPerWarp; ++r) {
-            float2 c0 = __fmul2_rn(a[0], g[r].w[0]);
+            float2 c0 = F::kOffset ? __ffma2_rn(a[0], g[r].w[0], c00) : __fmul2_rn(a[0], g[r].w[0]);
             float2 c1 = __fmul2_rn(a[4], g[r].w[4]);
             c0 = __ffma2_rn(a[1], g[r].w[1], c0);
             c1 = __ffma2_rn(a[5], g[r].w[5], c1);
@@ -299,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, (ScalarCfg<F, M, ARES>::kMinBlocks))
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       const float v = warp_sum(acc[r][m].x + acc[r][m].y);
-      if (lane == m && r0 + r < rows) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(v);
+      if (lane == m && r0 + r < rows) p.C[static_cast<size_t>(m) * p.ldc + n] = f32_to_bf16_rn(v * F::kOutScale);
     }
   }
 }
@@ -316,7 +336,7 @@ cudaError_t launch_scalar_m(const GemvArgs& a, cudaStream_t s) {
   auto kern = gemv_scalar_kernel<F, M, BULK, ARES>;
   static AttrLatch latch;
   if (cudaError_t e0 = set_smem_attrs(kern, latch, Cfg::kSmemMax, false); e0 != cudaSuccess) return e0;
-  const int smem = Cfg::kSmemFixed + (ARES ? M * a.K * 4 : 0);
+  const int smem = Cfg::kSmemFixed + (ARES ? M * a.K * 4 + (F::kOffset ? M * (a.K / 16) * 4 : 0) : 0);
   CUtensorMap mw = {}, mw2 = {}, ma = {};
   cudaError_t e = cudaSuccess;
   if (!ARES && (e = make_act_map(&ma, a, Cfg::kAW)) != cudaSuccess) return e;

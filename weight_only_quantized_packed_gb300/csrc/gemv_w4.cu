@@ -7,9 +7,9 @@
 namespace wqp {
 
 struct W4Fmt {
-  static constexpr int kTK = 512;                  // 4 groups per stage
-  static constexpr int kWRow = 256;                // code bytes of 512 K
-  static constexpr int kW2Row = 32;                // E4M3 scale bytes of 512 K
+  static constexpr int kTK = 1024;                 // 8 groups per stage
+  static constexpr int kWRow = 512;                // code bytes of 1024 K
+  static constexpr int kW2Row = 64;                // E4M3 scale bytes of 1024 K
   // Scale rows are K/16 bytes: a multiple of 16 iff K % 256 == 0.
   static bool bulk_ok(int K) { return K % 256 == 0; }
   static cudaError_t make_maps(const GemvArgs& a, CUtensorMap* mw, CUtensorMap* ms) {
@@ -26,13 +26,15 @@ struct W4Fmt {
   __device__ static void copy_row_plain(const ScalarParams& p, int n, int t, int tg, uint8_t* dst,
                                         uint8_t* dst2, int lane) {
     const size_t K = static_cast<size_t>(p.K);
-    const uint32_t* c = reinterpret_cast<const uint32_t*>(p.W + n * (K / 2) + 256 * t);
+    const uint32_t* c = reinterpret_cast<const uint32_t*>(p.W + n * (K / 2) + kWRow * t);
     for (int i = lane; i < 16 * tg; i += 32) reinterpret_cast<uint32_t*>(dst)[i] = __ldg(c + i);
     const uint16_t* sc =
-        reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(p.scales) + n * (K / 16) + 32 * t);
+        reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(p.scales) + n * (K / 16) + kW2Row * t);
     for (int i = lane; i < 4 * tg; i += 32) reinterpret_cast<uint16_t*>(dst2)[i] = __ldg(sc + i);
   }
   __device__ static constexpr float prescale(int) { return 1.0f; }
+  static constexpr bool kOffset = false;
+  static constexpr float kOutScale = 1.0f;
   // Segment sg = K elements [16 sg, 16 sg + 16) of the tile: 8 code bytes and
   // the one E4M3 scale of that 16-group.
   __device__ static void decode(const ScalarParams& p, int, int, int sg, const uint8_t* sW,

@@ -28,6 +28,8 @@ struct W8Fmt {
     for (int i = lane; i < 8 * tg; i += 32) reinterpret_cast<uint4*>(dst)[i] = __ldg(c + i);
   }
   __device__ static constexpr float prescale(int) { return 1.0f; }
+  static constexpr bool kOffset = false;
+  static constexpr float kOutScale = 1.0f;
   __device__ static void decode(const ScalarParams& p, int n, int t, int sg, const uint8_t* sW, const uint8_t*,
                                 Seg& g) {
     const uint4 c = *reinterpret_cast<const uint4*>(sW + 16 * sg);
