@@ -22,14 +22,17 @@
 // tile. Clusters are persistent: cluster c handles tiles c, c + C, c + 2C, ...
 // and each CTA streams its (tile, stage) items through a ring of raw stages.
 //
-// Warps of a CTA:
-//   0..7  compute: warp w owns block w of every stage, for all four 16-row
-//         tiles; after the grid-dependency wait it builds the MMA B fragments
-//         of its blocks once per call (in registers when the rank owns one
-//         stage, else in shared memory) and then only decodes codes and
-//         issues MMAs. At the end of a tile it hands its sums to the epilogue;
-//   8     producer: TMA of the raw stages (64 rows x 272 bytes) into the ring;
-//   9     epilogue: adds the 8 warps' sums of a tile (warp order); ranks >= 1
+// Warps of a CTA (W = 8 compute warps when several CTAs share an SM, 16
+// when one CTA has the SM):
+//   0..W-1 compute: warp w owns block w % 8 of every stage, for all four
+//         16-row tiles (W = 8) or two of them (W = 16); after the
+//         grid-dependency wait the MMA B fragments of its blocks are built
+//         once per call (in registers when the rank owns one stage, else in
+//         shared memory by the block's first warp) and then it only decodes
+//         codes and issues MMAs. At the end of a tile it hands its sums to
+//         the epilogue;
+//   W     producer: TMA of the raw stages (64 rows x 272 bytes) into the ring;
+//   W+1   epilogue: adds the 8 blocks' sums of a tile (block order); ranks >= 1
 //         send the result to rank 0 with st.async (completing on rank 0's
 //         mbarrier), rank 0 adds them in rank order and stores C. A one-slot
 //         receive buffer with a "free" barrier per peer (arrived from rank 0)
@@ -67,10 +70,11 @@ namespace mmas {
 
 constexpr int BM = 64;                       // weight rows per tile
 constexpr int kTiles = 4;                    // 16-row MMA tiles per tile
-constexpr int kCompute = 8;                  // compute warps: one per 128-K block of a stage
-constexpr int kProducer = kCompute;          // warp index of the TMA producer
-constexpr int kEpilogue = kCompute + 1;      // warp index of the epilogue
-constexpr int kThreads = (kCompute + 2) * 32;
+// Compute warps: one per 128-K block of a stage and all four row tiles when
+// several CTAs share an SM; with one CTA per SM two per block, each with two
+// of the row tiles (more warps to hide the mask -> MMA latencies).
+constexpr int compute_warps(int occ) { return occ == 1 ? 16 : 8; }
+constexpr int threads_for(int occ) { return (compute_warps(occ) + 2) * 32; }
 constexpr int kBlocks = 8;                   // 128-K blocks per raw stage (1024 K)
 constexpr int kRowBytes = kBlocks * 34;      // 272: 17 x 16 bytes
 constexpr int kStageBytes = BM * kRowBytes;  // 17408
@@ -82,7 +86,7 @@ template <int MT>
 struct Sizes {
   static constexpr int kItems = kTiles * MT * 32;   // float4 sums of one warp for one tile
   static constexpr int kSlot = kItems * 16;          // one rank's sums of a tile (bytes)
-  static constexpr int kRed = kCompute * kSlot;      // every compute warp's sums of a tile
+  static constexpr int kRed = kBlocks * kSlot;       // every block's sums of a tile
   static constexpr int kBf = MT * 32 * 64;           // B fragments of one block (16 words per lane per m tile)
   static constexpr int kNs = MT * 32 * 8;            // offset-chain pair of one block
 };
@@ -204,9 +208,13 @@ __device__ __forceinline__ void build_bfrag(const StreamParams& p, int kb, int m
 //        kept in shared memory, one set per stage of the rank.
 // kOcc: CTAs per SM the registers are budgeted for.
 template <int MT, bool kRegB, int kOcc>
-__global__ void __launch_bounds__(kThreads, kOcc)
+__global__ void __launch_bounds__(threads_for(kOcc), kOcc)
     q2_stream_kernel(const __grid_constant__ CUtensorMap tmW, const StreamParams p) {
   using Z = Sizes<MT>;
+  constexpr int kCW = compute_warps(kOcc);        // compute warps
+  constexpr int kTPW = kTiles * kBlocks / kCW;    // row tiles per compute warp (4 or 2)
+  constexpr int kProducer = kCW;                  // warp index of the TMA producer
+  constexpr int kEpilogue = kCW + 1;              // warp index of the epilogue
   extern __shared__ __align__(1024) uint8_t smem[];
   // full[R], empty[R], red_full, red_empty, recv_full[2], recv_free[2]
   __shared__ __align__(8) uint64_t bars[2 * kMaxRing + 6];
@@ -227,9 +235,9 @@ __global__ void __launch_bounds__(kThreads, kOcc)
   if (threadIdx.x == 0) {
     for (int i = 0; i < R; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, kCompute);
+      mbar_init(empty0 + 8 * i, kCW);
     }
-    mbar_init(red_full, kCompute);
+    mbar_init(red_full, kCW);
     mbar_init(red_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(recv_full + 8 * i, 1);
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, kOcc)
         const int item = i * 32 + lane;            // (row tile, column tile, lane) of a warp's sums
         v[i] = red[item];
 #pragma unroll
-        for (int w = 1; w < kCompute; ++w) {     // warp (block) order
+        for (int w = 1; w < kBlocks; ++w) {      // block order
           const float4 u = red[w * Z::kItems + item];
           v[i].x += u.x;
           v[i].y += u.y;
@@ -343,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, kOcc)
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int b = warp;                           // block b of every stage
+    const int b = warp % kBlocks;                 // block b of every stage
+    const int rq = warp / kBlocks;                // row tiles rq * kTPW .. + kTPW - 1
     const int g = lane >> 2, t4 = lane & 3;
     if (S > 1) tc::cluster_wait();
     pdl_wait();                                   // activations may belong to the previous grid
@@ -355,35 +364,39 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) build_bfrag(p, (st0 * kBlocks + b) * 128, mt, g, t4, bf[mt], ns[mt]);
     } else {
-      // One set per stage of the rank, written and read by this warp only.
-      for (int j = 0; j < nst; ++j) {
+      // One set per stage of the rank and block, written by the block's
+      // first warp and read by the block's warps.
+      for (int j = 0; j < nst && rq == 0; ++j) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           build_bfrag(p, ((st0 + j) * kBlocks + b) * 128, mt, g, t4, bf[mt], ns[mt]);
-          const int set = (j * kCompute + b) * MT + mt;
+          const int set = (j * kBlocks + b) * MT + mt;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             bfs[(set * 4 + q) * 32 + lane] = make_uint4(bf[mt][4 * q], bf[mt][4 * q + 1], bf[mt][4 * q + 2], bf[mt][4 * q + 3]);
           nss[set * 32 + lane] = make_float2(ns[mt][0], ns[mt][1]);
         }
       }
-      __syncwarp();
+      if constexpr (kCW > kBlocks)
+        asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");   // every set written
+      else
+        __syncwarp();
     }
     // Row tiles whose MMA chains run interleaved: all four when registers
     // allow, else two at a time.
-    constexpr int kG = (kOcc >= 3 || MT == 2) ? 2 : kTiles;
+    constexpr int kG = (kOcc >= 3 || MT == 2) ? 2 : kTPW;
     // Sums across the rank's stages of a tile (a rank with one stage writes
     // each item's sums straight to the epilogue's buffer instead).
-    float tot[kRegB ? 1 : kTiles][MT][4];
+    float tot[kRegB ? 1 : kTPW][MT][4];
     if constexpr (!kRegB) {
 #pragma unroll
-      for (int rt = 0; rt < kTiles; ++rt)
+      for (int rt = 0; rt < kTPW; ++rt)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
           for (int i = 0; i < 4; ++i) tot[rt][mt][i] = 0.f;
     }
-    float4* red = reinterpret_cast<float4*>(smem + p.red_off) + warp * Z::kItems;
+    float4* red = reinterpret_cast<float4*>(smem + p.red_off) + b * Z::kItems;
     bool live = true;
     auto run = [&](auto ac) {
       constexpr int kA = decltype(ac)::value;
@@ -394,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, kOcc)
           if (nst > 1 || it == 0) {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              const int set = (j * kCompute + b) * MT + mt;
+              const int set = (j * kBlocks + b) * MT + mt;
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const uint4 u = bfs[(set * 4 + q) * 32 + lane];
@@ -416,9 +429,9 @@ __global__ void __launch_bounds__(kThreads, kOcc)
         }
         live = __all_sync(0xFFFFFFFFu, live);
         if (live) {
-          const uint8_t* blk = smem + s * kStageBytes + g * kRowBytes + 34 * b;
+          const uint8_t* blk = smem + s * kStageBytes + (16 * kTPW * rq + g) * kRowBytes + 34 * b;
 #pragma unroll
-          for (int r0 = 0; r0 < kTiles; r0 += kG) {
+          for (int r0 = 0; r0 < kTPW; r0 += kG) {
             uint32_t wg[kG][2], wh[kG][2];        // code words 2t, 2t + 1 of rows g, g + 8
             float dg[kG], dh[kG];
             float c[kG][MT][4];
@@ -461,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
                 if constexpr (kRegB) {
-                  red[((r0 + i) * MT + mt) * 32 + lane] =
+                  red[((kTPW * rq + r0 + i) * MT + mt) * 32 + lane] =
                       make_float4(dg[i] * c[i][mt][0], dg[i] * c[i][mt][1], dh[i] * c[i][mt][2], dh[i] * c[i][mt][3]);
                 } else {
                   float* t = tot[r0 + i][mt];
@@ -486,10 +499,11 @@ __global__ void __launch_bounds__(kThreads, kOcc)
             if (tl > 0 && live) live = tc::wait_or_abort(red_empty, (tl - 1) & 1, p.err, abort_flag);
             live = __all_sync(0xFFFFFFFFu, live);
 #pragma unroll
-            for (int rt = 0; rt < kTiles; ++rt)
+            for (int rt = 0; rt < kTPW; ++rt)
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
-                red[(rt * MT + mt) * 32 + lane] = make_float4(tot[rt][mt][0], tot[rt][mt][1], tot[rt][mt][2], tot[rt][mt][3]);
+                red[((kTPW * rq + rt) * MT + mt) * 32 + lane] =
+                    make_float4(tot[rt][mt][0], tot[rt][mt][1], tot[rt][mt][2], tot[rt][mt][3]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) tot[rt][mt][i] = 0.f;
               }
@@ -544,7 +558,7 @@ int cluster_capacity(int s) {
   using V = Variant<MT, kRegB, kOcc>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(s);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(kOcc));
   cfg.dynamicSmemBytes = V::kBudget;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -576,7 +590,7 @@ template <int MT>
 void layout(Plan& pl, int stages, int budget) {
   using Z = Sizes<MT>;
   const int nsmax = (stages + pl.splits - 1) / pl.splits;
-  const int bfsets = pl.regb ? 0 : nsmax * kCompute * MT;
+  const int bfsets = pl.regb ? 0 : nsmax * kBlocks * MT;
   const int fixed = Z::kRed + 2 * (pl.splits - 1) * Z::kSlot + bfsets * (32 * 64 + 32 * 8);
   pl.ring = std::min(kMaxRing, (budget - fixed) / kStageBytes);
   pl.red_off = pl.ring * kStageBytes;
@@ -663,7 +677,7 @@ cudaError_t launch_variant(const CUtensorMap& mw, const StreamParams& p, bool pd
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.clusters * p.splits);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(kOcc));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
