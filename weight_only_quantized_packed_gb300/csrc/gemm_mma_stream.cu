@@ -207,7 +207,10 @@ __device__ __forceinline__ void build_bfrag(const StreamParams& p, int kb, int m
 //        fragments stay in registers for the whole call; otherwise they are
 //        kept in shared memory, one set per stage of the rank.
 // kOcc: CTAs per SM the registers are budgeted for.
-template <int MT, bool kRegB, int kOcc>
+// kPair: no K split, and the two CTAs of a cluster share the B-fragment
+//        sets (each stores those of every other stage), for 16-row calls
+//        whose sets would not fit one CTA.
+template <int MT, bool kRegB, int kOcc, bool kPair = false>
 __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
     q2_stream_kernel(const __grid_constant__ CUtensorMap tmW, const StreamParams p) {
   using Z = Sizes<MT>;
@@ -222,6 +225,11 @@ __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
   volatile int* abort_flag = &abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.splits, C = p.clusters, R = p.ring;
+  // Paired CTAs (S = 1): each stores the B-fragment sets of every other stage
+  // and reads the rest from its peer's shared memory.
+  constexpr bool pair = kPair && !kRegB;
+  const bool clustered = S > 1 || pair;
+  const int prk = pair ? static_cast<int>(tc::cluster_rank()) : 0;
   const int cl = blockIdx.x / S;
   const int rank = blockIdx.x - cl * S;           // == %cluster_ctarank
   const int st0 = (rank * p.stages) / S;
@@ -246,13 +254,19 @@ __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
     mbar_fence_init();
     abort_sh = 0;
   }
-  if (S > 1) tc::cluster_arrive_relaxed();
+  if (clustered) tc::cluster_arrive_relaxed();
   __syncthreads();
   pdl_launch_dependents();
 
   if (warp == kProducer) {
     // ------------------------------------------------------------ producer
     // Weights do not depend on the previous grid: the copies start at once.
+    if (pair) {
+      // The second cluster barrier (B-fragment sets written) must not wait
+      // on this warp's copies: arrive now, wait at the end.
+      tc::cluster_wait();
+      tc::cluster_arrive();
+    }
     if (lane == 0) {
       tc::prefetch_tmap(&tmW);
       const uint64_t pol = policy_evict_first();
@@ -271,10 +285,11 @@ __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
       for (int it = max(0, issued - R); it < issued; ++it) mbar_wait(full0 + 8 * (it % R), (it / R) & 1, p.err);
     }
     __syncwarp();
-    if (S > 1) tc::cluster_wait();
+    if (clustered) tc::cluster_wait();
   } else if (warp == kEpilogue) {
     // ------------------------------------------------------------ epilogue
-    if (S > 1) tc::cluster_wait();                     // every rank's barriers are initialised
+    if (clustered) tc::cluster_wait();                 // every rank's barriers are initialised
+    if (pair) tc::cluster_arrive();                    // second barrier: waited at the end
     pdl_wait();                                    // C may be read by the previous grid
     const float4* red = reinterpret_cast<const float4*>(smem + p.red_off);
     const float4* recv = reinterpret_cast<const float4*>(smem + p.recv_off);
@@ -349,12 +364,13 @@ __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
         }
       }
     }
+    if (pair) tc::cluster_wait();
   } else {
     // ------------------------------------------------------------ compute
     const int b = warp % kBlocks;                 // block b of every stage
     const int rq = warp / kBlocks;                // row tiles rq * kTPW .. + kTPW - 1
     const int g = lane >> 2, t4 = lane & 3;
-    if (S > 1) tc::cluster_wait();
+    if (clustered) tc::cluster_wait();
     pdl_wait();                                   // activations may belong to the previous grid
     uint32_t bf[MT][16];
     float ns[MT][2];
@@ -365,12 +381,15 @@ __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
       for (int mt = 0; mt < MT; ++mt) build_bfrag(p, (st0 * kBlocks + b) * 128, mt, g, t4, bf[mt], ns[mt]);
     } else {
       // One set per stage of the rank and block, written by the block's
-      // first warp and read by the block's warps.
+      // first warp and read by the block's warps (paired CTAs: stage j's set
+      // lives in CTA j % 2 of the pair, at index j / 2).
       for (int j = 0; j < nst && rq == 0; ++j) {
+        if (pair && (j & 1) != prk) continue;
+        const int jl = pair ? (j >> 1) : j;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           build_bfrag(p, ((st0 + j) * kBlocks + b) * 128, mt, g, t4, bf[mt], ns[mt]);
-          const int set = (j * kBlocks + b) * MT + mt;
+          const int set = (jl * kBlocks + b) * MT + mt;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             bfs[(set * 4 + q) * 32 + lane] = make_uint4(bf[mt][4 * q], bf[mt][4 * q + 1], bf[mt][4 * q + 2], bf[mt][4 * q + 3]);
@@ -381,6 +400,10 @@ __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
         asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");   // every set written
       else
         __syncwarp();
+      if (pair) {                                 // and the peer's
+        tc::cluster_arrive();
+        tc::cluster_wait();
+      }
     }
     // Row tiles whose MMA chains run interleaved: all four when registers
     // allow, else two at a time.
@@ -405,18 +428,22 @@ __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
       for (int it = 0; it < items; ++it) {
         if constexpr (!kRegB) {
           if (nst > 1 || it == 0) {
+            const int jl = pair ? (j >> 1) : j;
+            const bool remote = pair && (j & 1) != prk;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              const int set = (j * kBlocks + b) * MT + mt;
+              const int set = (jl * kBlocks + b) * MT + mt;
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const uint4 u = bfs[(set * 4 + q) * 32 + lane];
+                const uint4 u = remote ? tc::ld_dsmem_v4(tc::mapa_shared(smem_u32(&bfs[(set * 4 + q) * 32 + lane]), j & 1))
+                                       : bfs[(set * 4 + q) * 32 + lane];
                 bf[mt][4 * q] = u.x;
                 bf[mt][4 * q + 1] = u.y;
                 bf[mt][4 * q + 2] = u.z;
                 bf[mt][4 * q + 3] = u.w;
               }
-              const float2 n2 = nss[set * 32 + lane];
+              const float2 n2 = remote ? tc::ld_dsmem_f2(tc::mapa_shared(smem_u32(&nss[set * 32 + lane]), j & 1))
+                                       : nss[set * 32 + lane];
               ns[mt][0] = n2.x;
               ns[mt][1] = n2.y;
             }
@@ -524,7 +551,7 @@ __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
   // Every CTA of the cluster stays until all are done: peers' st.async into
   // rank 0's shared memory and rank 0's arrives on the peers' barriers have
   // all landed before any CTA exits.
-  if (S > 1) tc::cluster_sync();
+  if (clustered) tc::cluster_sync();
 }
 
 // ---------------------------------------------------------------- host side
@@ -532,22 +559,23 @@ constexpr int kBudget3 = 74 * 1024;    // dynamic shared memory of a 3-CTA-per-S
 constexpr int kBudget2 = 110 * 1024;   // of a 2-CTA-per-SM variant
 constexpr int kBudget1 = 220 * 1024;   // of a 1-CTA-per-SM variant
 
-template <int MT, bool kRegB, int kOcc>
+template <int MT, bool kRegB, int kOcc, bool kPair = false>
 struct Variant {
-  static constexpr auto kernel = q2_stream_kernel<MT, kRegB, kOcc>;
+  static constexpr auto kernel = q2_stream_kernel<MT, kRegB, kOcc, kPair>;
   static constexpr int kBudget = kOcc == 3 ? kBudget3 : (kOcc == 2 ? kBudget2 : kBudget1);
 };
 
 // Dynamic shared memory opt-in and the whole carveout, once per device.
-template <int MT, bool kRegB, int kOcc>
+template <int MT, bool kRegB, int kOcc, bool kPair = false>
 cudaError_t set_attrs() {
   static AttrLatch latch;
-  return set_smem_attrs(Variant<MT, kRegB, kOcc>::kernel, latch, Variant<MT, kRegB, kOcc>::kBudget, true);
+  using V = Variant<MT, kRegB, kOcc, kPair>;
+  return set_smem_attrs(V::kernel, latch, V::kBudget, true);
 }
 
 // Clusters of s CTAs of a variant resident at once (0 if the query failed),
 // with the variant's shared-memory budget. Cached per device.
-template <int MT, bool kRegB, int kOcc>
+template <int MT, bool kRegB, int kOcc, bool kPair = false>
 int cluster_capacity(int s) {
   static std::atomic<int> cache[kMaxDevices][kMaxSplits + 1];
   int dev = 0;
@@ -555,7 +583,7 @@ int cluster_capacity(int s) {
   std::atomic<int>& slot = cache[dev][s];
   int v = slot.load(std::memory_order_relaxed);
   if (v != 0) return v > 0 ? v : 0;
-  using V = Variant<MT, kRegB, kOcc>;
+  using V = Variant<MT, kRegB, kOcc, kPair>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(s);
   cfg.blockDim = dim3(threads_for(kOcc));
@@ -568,7 +596,7 @@ int cluster_capacity(int s) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (set_attrs<MT, kRegB, kOcc>() != cudaSuccess || cudaOccupancyMaxActiveClusters(&n, V::kernel, &cfg) != cudaSuccess) {
+  if (set_attrs<MT, kRegB, kOcc, kPair>() != cudaSuccess || cudaOccupancyMaxActiveClusters(&n, V::kernel, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();            // the query's failure is not the caller's error
     n = 0;
   }
@@ -582,6 +610,7 @@ struct Plan {
   bool regb = false;
   int occ = 2;
   int splits = 1, clusters = 1, ring = 2;
+  bool pair = false;   // no K split; the two CTAs of a cluster share the B-fragment sets
   int red_off = 0, recv_off = 0, bf_off = 0, ns_off = 0, smem = 0;
   double cost = -1.0;
 };
@@ -590,7 +619,7 @@ template <int MT>
 void layout(Plan& pl, int stages, int budget) {
   using Z = Sizes<MT>;
   const int nsmax = (stages + pl.splits - 1) / pl.splits;
-  const int bfsets = pl.regb ? 0 : nsmax * kBlocks * MT;
+  const int bfsets = pl.regb ? 0 : (pl.pair ? (nsmax + 1) / 2 : nsmax) * kBlocks * MT;
   const int fixed = Z::kRed + 2 * (pl.splits - 1) * Z::kSlot + bfsets * (32 * 64 + 32 * 8);
   pl.ring = std::min(kMaxRing, (budget - fixed) / kStageBytes);
   pl.red_off = pl.ring * kStageBytes;
@@ -610,20 +639,31 @@ constexpr double kSmRate[4] = {0.0, 1.0, 1.15, 1.45};
 constexpr double kSplitTileCost = 0.35;
 
 template <int MT, bool kRegB, int kOcc>
-void consider(Plan& best, int splits, int tiles, int stages, int num_sms) {
+void consider(Plan& best, int splits, int tiles, int stages, int num_sms, bool pair = false) {
+  if (pair && (kRegB || splits != 1)) return;
   Plan pl;
   pl.mt = MT;
   pl.regb = kRegB;
   pl.occ = kOcc;
   pl.splits = splits;
+  pl.pair = pair;
   layout<MT>(pl, stages, Variant<MT, kRegB, kOcc>::kBudget);
   if (pl.ring < 2) return;
   const int nsmax = (stages + splits - 1) / splits;
-  const int cap = cluster_capacity<MT, kRegB, kOcc>(splits);
+  // Paired plans: clusters of two CTAs; pl.clusters counts CTAs (even).
+  const int csize = pair ? 2 : splits;
+  int cap = 0;
+  if constexpr (MT == 2 && !kRegB && kOcc == 1) {   // the only paired variant
+    cap = pair ? cluster_capacity<MT, false, kOcc, true>(2) : cluster_capacity<MT, kRegB, kOcc>(csize);
+  } else {
+    if (pair) return;
+    cap = cluster_capacity<MT, kRegB, kOcc>(csize);
+  }
   // At most two CTAs of the call per SM: the next call's CTAs find a free
   // slot on every SM and load their weights while this call finishes.
-  const int clusters = std::min({tiles, cap > 0 ? cap : (kOcc * num_sms) / splits, (2 * num_sms) / splits});
-  if (clusters < 1) return;
+  int clusters = pair ? std::min({tiles, cap > 0 ? 2 * cap : kOcc * num_sms, 2 * num_sms}) & ~1
+                      : std::min({tiles, cap > 0 ? cap : (kOcc * num_sms) / splits, (2 * num_sms) / splits});
+  if (clusters < (pair ? 2 : 1)) return;
   pl.clusters = clusters;
   // Work of the busiest SM, in (tile, stage) items of 64 x 1024 weights,
   // over the rate of an SM holding that many CTAs.
@@ -651,6 +691,10 @@ Plan choose_plan(int tiles, int stages, int num_sms, int only_splits = 0) {
       consider<MT, false, 1>(best, s, tiles, stages, num_sms);
     }
   }
+  // Two column tiles with no K split need the B fragments of both for every
+  // stage; when they do not fit, a pair of CTAs shares them.
+  if (MT == 2 && best.cost < 0 && only_splits <= 1 && stages > 1)
+    consider<MT, false, 1>(best, 1, tiles, stages, num_sms, true);
   return best;
 }
 
@@ -671,9 +715,9 @@ PlanCache& plan_cache() {
   return c;
 }
 
-template <int MT, bool kRegB, int kOcc>
+template <int MT, bool kRegB, int kOcc, bool kPair = false>
 cudaError_t launch_variant(const CUtensorMap& mw, const StreamParams& p, bool pdl, int smem, cudaStream_t s) {
-  cudaError_t e = set_attrs<MT, kRegB, kOcc>();
+  cudaError_t e = set_attrs<MT, kRegB, kOcc, kPair>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.clusters * p.splits);
@@ -683,7 +727,7 @@ cudaError_t launch_variant(const CUtensorMap& mw, const StreamParams& p, bool pd
   cudaLaunchAttribute attr[2];
   int na = 0;
   attr[na].id = cudaLaunchAttributeClusterDimension;
-  attr[na].val.clusterDim.x = p.splits;
+  attr[na].val.clusterDim.x = kPair ? 2 : p.splits;
   attr[na].val.clusterDim.y = 1;
   attr[na].val.clusterDim.z = 1;
   ++na;
@@ -694,7 +738,7 @@ cudaError_t launch_variant(const CUtensorMap& mw, const StreamParams& p, bool pd
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, Variant<MT, kRegB, kOcc>::kernel, mw, p);
+  return cudaLaunchKernelEx(&cfg, Variant<MT, kRegB, kOcc, kPair>::kernel, mw, p);
 }
 
 }  // namespace mmas
@@ -772,6 +816,7 @@ cudaError_t launch_q2_gemm_stream(const GemvArgs& a, cudaStream_t s) {
     return launch_variant<1, false, 1>(mw, p, a.pdl, pl.smem, s);
   }
   if (pl.regb) return launch_variant<2, true, 2>(mw, p, a.pdl, pl.smem, s);
+  if (pl.pair) return launch_variant<2, false, 1, true>(mw, p, a.pdl, pl.smem, s);
   return launch_variant<2, false, 1>(mw, p, a.pdl, pl.smem, s);
 }
 
