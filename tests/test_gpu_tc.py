@@ -189,6 +189,19 @@ def test_q2_mma_persistent_rows_independent():
         assert np.array_equal(one[0], c16[m]), m
 
 
+def test_q2_mma_paired_ragged(oracle_lib):
+    """A ragged shape on the persistent kernel's paired 16-row plan (no K
+    split, B fragments shared by two CTAs): N = 20001 leaves a partial last
+    tile; parity with the oracle, and rows equal to the rows computed alone."""
+    N, K = 20001, 5120
+    d = G.make("q2", 16, N, K, seed=31)
+    c16 = G.host_bits(G.run_gpu(d, tc="mma"))
+    _check_tc(oracle_lib, d, c16, f"q2 paired M=16 N={N} K={K} mma")
+    for m in (0, 7, 8, 15):
+        one = G.host_bits(G.run_gpu(d, tc="mma", A=d["dA"][m:m + 1]))
+        assert np.array_equal(one[0], c16[m]), m
+
+
 @ENGINES
 def test_q2_tc_activation_range(oracle_lib, eng):
     """The pre-scale 2^(64 - 2j) stays exact for large and small activations
