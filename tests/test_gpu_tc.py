@@ -189,6 +189,20 @@ def test_q2_mma_persistent_rows_independent():
         assert np.array_equal(one[0], c16[m]), m
 
 
+def test_q2_mma_tall_tiles_ragged(oracle_lib):
+    """A shape whose single-stage grid of 64-row CTAs would need a fourth CTA
+    slot per SM runs as 96-row CTAs (N = 7000, K = 5120: a partial last
+    96-row tile and a partial 16-row tile); parity with the oracle, and rows
+    equal to the rows computed alone."""
+    N, K = 7000, 5120
+    d = G.make("q2", 8, N, K, seed=33)
+    c8 = G.host_bits(G.run_gpu(d, tc="mma"))
+    _check_tc(oracle_lib, d, c8, f"q2 96-row tiles M=8 N={N} K={K} mma")
+    for m in (0, 3, 7):
+        one = G.host_bits(G.run_gpu(d, tc="mma", A=d["dA"][m:m + 1]))
+        assert np.array_equal(one[0], c8[m]), m
+
+
 def test_q2_mma_paired_ragged(oracle_lib):
     """A ragged shape on the persistent kernel's paired 16-row plan (no K
     split, B fragments shared by two CTAs): N = 20001 leaves a partial last

@@ -18,10 +18,10 @@
 // words into MMA operands in registers and issues the MMAs itself, so nothing
 // waits on another warp until the stage's sums are added.
 //
-// Layout of one CTA (BM = 64 weight rows x the CTA's K range):
+// Layout of one CTA (BM = 64 or 96 weight rows x the CTA's K range):
 //   warps 0..7  compute: warp w owns block w (128 K) of every stage, for all
-//               four 16-row tiles of the CTA;
-//   warp 8      producer: TMA of raw stages (64 rows x 8 blocks x 34 bytes).
+//               BM / 16 row tiles of the CTA;
+//   warp 8      producer: TMA of raw stages (BM rows x 8 blocks x 34 bytes).
 // Per 128-K block b and thread (g = lane / 4, t = lane % 4):
 //   * A fragment: code words 2t and 2t + 1 of the block, rows g and g + 8 of
 //     a tile. Word bits 2q..2q+1 hold code q (q < 16). The pair of 16-bit
@@ -32,7 +32,7 @@
 //   * B fragment: activation row m = g (rows past M repeat row M - 1): the 32
 //     activations of k = 128 b + 32 t .. + 31, paired the same way and
 //     multiplied by 2^(64 - 2x), so every product is c * a * 2^-69 exactly.
-//     Built once per block, in registers, and used for all four tiles.
+//     Built once per block, in registers, and used for all row tiles.
 //   * Each tile's chain starts from -2^-69 * sum_k a (four MMAs per block
 //     with the raw activations as the A operand and -2^-69 as B, run once
 //     per block), so it ends at 2^-69 * sum_k (c - 1) a.
@@ -52,24 +52,25 @@
 namespace wqp {
 namespace mma {
 
-constexpr int BM = 64;                       // weight rows per CTA
-constexpr int kTiles = 4;                    // 16-row MMA tiles per CTA
-constexpr int kCompute = 2 * kTiles;         // compute warps: one per 128-K block of a stage (8)
-constexpr int kThreads = (kCompute + 1) * 32;
 constexpr int kBlocks = 8;                   // 128-K blocks per raw stage (1024 K)
+constexpr int kCompute = kBlocks;            // compute warps: one per 128-K block of a stage
+constexpr int kThreads = (kCompute + 1) * 32;
 constexpr int kRowBytes = kBlocks * 34;      // 272: 17 x 16 bytes
-constexpr int kStageBytes = BM * kRowBytes;  // 17408
 constexpr int kMaxSplits = 8;                // CTAs per cluster (K split) at most (portable size)
 
 // MT: m tiles of 8 activation rows per launch (1 is the one launched: a
 // 16-row form measured slower than two 8-row launches).
 // kMulti: a CTA runs more than one raw stage (two raw buffers, one refilled
 // while the other is consumed); otherwise exactly one.
-template <int MT, bool kMulti>
+// kBM: weight rows per CTA (64, or 96 for grids that would need a fourth
+// CTA slot per SM with 64).
+template <int MT, bool kMulti, int kBM>
 struct Cfg {
+  static constexpr int kTiles = kBM / 16;                        // 16-row MMA tiles
+  static constexpr int kStageBytes = kBM * kRowBytes;            // raw stage (17408 or 26112)
   static constexpr int SW = kMulti ? 2 : 1;                      // raw stage buffers
   static constexpr int kRawOff = 0;
-  // Every compute warp's partial sums (4 tiles x MT x 32 lanes x 4 floats),
+  // Every compute warp's partial sums (tiles x MT x 32 lanes x 4 floats),
   // written over the raw buffers once all of them are consumed.
   static constexpr int kSlot = kTiles * MT * 32 * 16;
   static constexpr int kRedOff = 0;
@@ -86,7 +87,8 @@ struct Cfg {
   static constexpr int kRecvOff = kActOff + kActBytes;            // ranks 1.. of the cluster, at rank 0
   // Dynamic shared memory for a cluster of `splits` CTAs.
   static constexpr int bytes(int splits) { return kRecvOff + (splits - 1) * kSlot; }
-  static_assert(kStageBytes % 1024 == 0 && kRecvOff % 16 == 0, "align");
+  static_assert(kBM % 16 == 0 && kStageBytes % 128 == 0 && kRecvOff % 16 == 0, "align");
+  static_assert(kTiles % 2 == 0, "row tiles run in pairs");
   static_assert(2 * (bytes(kMaxSplits) + 1024) <= 227 * 1024, "shared memory per SM");
 };
 
@@ -195,10 +197,12 @@ __device__ __forceinline__ void offset_sums(const uint32_t (&r)[16], int t4, flo
 }
 
 // kOcc: CTAs per SM the registers are budgeted for.
-template <int MT, bool kMulti, int kOcc>
+template <int MT, bool kMulti, int kOcc, int kBM>
 __global__ void __launch_bounds__(kThreads, kOcc)
     q2_mma_kernel(const __grid_constant__ CUtensorMap tmW, const MmaParams p) {
-  using L = Cfg<MT, kMulti>;
+  using L = Cfg<MT, kMulti, kBM>;
+  constexpr int kTiles = L::kTiles;
+  constexpr int kStageBytes = L::kStageBytes;
   constexpr int SW = L::SW;
   extern __shared__ __align__(1024) uint8_t smem[];
   // full[SW], empty[SW], partial sums received, activation rows landed
@@ -209,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, kOcc)
   const int splits = p.splits;
   const int tile = blockIdx.x / splits;
   const int rank = blockIdx.x - tile * splits;   // == %cluster_ctarank
-  const int n0 = tile * BM;
+  const int n0 = tile * kBM;
   const int st0 = (rank * p.stages) / splits;
   const int T = kMulti ? ((rank + 1) * p.stages) / splits - st0 : 1;   // >= 1: splits <= stages
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[SW]), recv_bar = smem_u32(&bars[2 * SW]);
@@ -315,9 +319,9 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 
   load_act(0);
   bool live = true;
-  // One m tile at a time: its B fragments and offset, then the four
-  // row tiles against them (for M > 8 the codes are decoded once per m tile,
-  // which keeps a single set of fragments live).
+  // One m tile at a time: its B fragments and offset, then every row tile
+  // against them (for M > 8 the codes are decoded once per m tile, which
+  // keeps a single set of fragments live).
   auto run = [&](auto ac) {
     constexpr int kA = decltype(ac)::value;
     for (int t = 0; t < T; ++t) {
@@ -490,26 +494,27 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 }
 
 // ---------------------------------------------------------------- host side
-// The compiled variants: (m tiles, several stages per CTA, CTAs per SM).
-// Single-stage M <= 8 calls have two register budgets: 3 CTAs per SM (63
-// registers) and 4 (56 registers) for grids that need the fourth slot.
-template <int MT, bool kMulti, int kOcc>
+// The compiled variants: (m tiles, several stages per CTA, CTAs per SM, rows
+// per CTA). Single-stage calls run 64-row CTAs three to an SM; a grid that
+// does not fit that runs 96-row CTAs three to an SM when those fit, else
+// 64-row CTAs four to an SM (56 registers).
+template <int MT, bool kMulti, int kOcc, int kBM>
 struct Variant {
-  static constexpr auto kernel = q2_mma_kernel<MT, kMulti, kOcc>;
+  static constexpr auto kernel = q2_mma_kernel<MT, kMulti, kOcc, kBM>;
 };
 
 // Opt-in shared memory above 48 KB (up to the largest cluster's size) and the
 // whole carveout (several CTAs per SM). Set once, before the first launch or
 // occupancy query.
-template <int MT, bool kMulti, int kOcc>
+template <int MT, bool kMulti, int kOcc, int kBM>
 cudaError_t set_attrs() {
   static AttrLatch latch;
-  return set_smem_attrs(Variant<MT, kMulti, kOcc>::kernel, latch, Cfg<MT, kMulti>::bytes(kMaxSplits), true);
+  return set_smem_attrs(Variant<MT, kMulti, kOcc, kBM>::kernel, latch, Cfg<MT, kMulti, kBM>::bytes(kMaxSplits), true);
 }
 
 // CTAs of a variant resident at once in clusters of s (0 if the query
 // failed). Cached per device.
-template <int MT, bool kMulti, int kOcc>
+template <int MT, bool kMulti, int kOcc, int kBM>
 int resident_ctas(int s) {
   static std::atomic<int> cache[kMaxDevices][kMaxSplits + 1];
   int dev = 0;
@@ -519,7 +524,7 @@ int resident_ctas(int s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(s);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<MT, kMulti>::bytes(s);
+  cfg.dynamicSmemBytes = Cfg<MT, kMulti, kBM>::bytes(s);
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = s;
@@ -528,8 +533,8 @@ int resident_ctas(int s) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (set_attrs<MT, kMulti, kOcc>() != cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, Variant<MT, kMulti, kOcc>::kernel, &cfg) != cudaSuccess) {
+  if (set_attrs<MT, kMulti, kOcc, kBM>() != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, Variant<MT, kMulti, kOcc, kBM>::kernel, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();            // the query's failure is not the caller's error
     n = 0;
   }
@@ -546,7 +551,7 @@ int choose_splits(int tiles, int stages, int num_sms) {
   long long best_cost = -1;
   for (int s = 1; s <= kMaxSplits && s <= stages; ++s) {
     const int per_cta = (stages + s - 1) / s;
-    int slots = per_cta > 1 ? resident_ctas<1, true, 3>(s) : resident_ctas<1, false, 4>(s);
+    int slots = per_cta > 1 ? resident_ctas<1, true, 3, 64>(s) : resident_ctas<1, false, 4, 64>(s);
     if (slots <= 0) slots = 3 * num_sms;
     const long long ctas = static_cast<long long>(tiles) * s;
     const long long waves = (ctas + slots - 1) / slots;
@@ -559,14 +564,14 @@ int choose_splits(int tiles, int stages, int num_sms) {
   return best;
 }
 
-template <int MT, bool kMulti, int kOcc>
+template <int MT, bool kMulti, int kOcc, int kBM>
 cudaError_t launch_variant(const CUtensorMap& mw, const MmaParams& p, int tiles, bool pdl, cudaStream_t s) {
-  cudaError_t e = set_attrs<MT, kMulti, kOcc>();
+  cudaError_t e = set_attrs<MT, kMulti, kOcc, kBM>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * p.splits);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<MT, kMulti>::bytes(p.splits);
+  cfg.dynamicSmemBytes = Cfg<MT, kMulti, kBM>::bytes(p.splits);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -582,7 +587,7 @@ cudaError_t launch_variant(const CUtensorMap& mw, const MmaParams& p, int tiles,
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, Variant<MT, kMulti, kOcc>::kernel, mw, p);
+  return cudaLaunchKernelEx(&cfg, Variant<MT, kMulti, kOcc, kBM>::kernel, mw, p);
 }
 
 }  // namespace mma
@@ -596,7 +601,7 @@ cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   // for up to 16 rows; B fragments built once per CTA). Otherwise one short
   // CTA per (tile, stage range) and 8 activation rows per launch. The choice
   // depends on the shape only, so a row's result does not depend on M.
-  if ((a.N + BM - 1) / BM >= 2 * a.num_sms) return launch_q2_gemm_stream(a, s);
+  if ((a.N + 63) / 64 >= 2 * a.num_sms) return launch_q2_gemm_stream(a, s);
   if (a.M > 8) {
     GemvArgs lo = a, hi = a;
     lo.M = 8;
@@ -607,10 +612,12 @@ cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s) {
     return e1 != cudaSuccess ? e1 : launch_q2_gemm_mma(hi, s);
   }
   const uint64_t G = static_cast<uint64_t>(a.K / 128);
+  // Raw stages of `bm` rows: boxes of 8 blocks x bm rows.
   CUtensorMap mw;
-  cudaError_t e = cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N),
-                                34 * G, kBlocks * 17, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (e != cudaSuccess) return e;
+  auto map = [&](int bm) {
+    return cached_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.W, 17 * G, static_cast<uint64_t>(a.N), 34 * G,
+                         kBlocks * 17, static_cast<uint32_t>(bm), CU_TENSOR_MAP_SWIZZLE_NONE);
+  };
   MmaParams p;
   p.A = static_cast<const uint16_t*>(a.A);
   p.C = static_cast<uint16_t*>(a.C);
@@ -622,17 +629,25 @@ cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   p.stages = a.K / (kBlocks * 128);
   p.splits = 1;
   p.err = a.err;
-  const int tiles = (a.N + BM - 1) / BM;
+  const int tiles = (a.N + 63) / 64;
   p.splits = choose_splits(tiles, p.stages, a.num_sms);
   const bool multi = (p.stages + p.splits - 1) / p.splits > 1;
+  cudaError_t e;
   // One 8-row activation tile (MT = 1): the C ABI calls this on 8-row chunks.
-  if (multi) return launch_variant<1, true, 3>(mw, p, tiles, a.pdl, s);
+  if (multi) return (e = map(64)) != cudaSuccess ? e : launch_variant<1, true, 3, 64>(mw, p, tiles, a.pdl, s);
   // Three CTAs per SM spread a grid that fits them over more SMs (the cluster
-  // scheduler fills an SM's free slots before the next SM's); four only when
-  // the grid needs the fourth slot to run in one wave.
-  const int ctas3 = resident_ctas<1, false, 3>(p.splits);
-  const bool fits3 = static_cast<long long>(tiles) * p.splits <= (ctas3 > 0 ? ctas3 : 3 * a.num_sms);
-  return fits3 ? launch_variant<1, false, 3>(mw, p, tiles, a.pdl, s) : launch_variant<1, false, 4>(mw, p, tiles, a.pdl, s);
+  // scheduler fills an SM's free slots before the next SM's). A grid of
+  // 64-row CTAs that does not fit runs as 96-row CTAs, three to an SM, when
+  // those fit in one wave (7168 x 5120: 5.4 -> 4.8 us at M = 1); else as
+  // 64-row CTAs four to an SM. The K split is the same in every case, so a
+  // row's summation order depends on K only.
+  auto fits = [&](int ctas, int slots) { return ctas <= (slots > 0 ? slots : 3 * a.num_sms); };
+  if (fits(tiles * p.splits, resident_ctas<1, false, 3, 64>(p.splits)))
+    return (e = map(64)) != cudaSuccess ? e : launch_variant<1, false, 3, 64>(mw, p, tiles, a.pdl, s);
+  const int tiles96 = (a.N + 95) / 96;
+  if (fits(tiles96 * p.splits, resident_ctas<1, false, 3, 96>(p.splits)))
+    return (e = map(96)) != cudaSuccess ? e : launch_variant<1, false, 3, 96>(mw, p, tiles96, a.pdl, s);
+  return (e = map(64)) != cudaSuccess ? e : launch_variant<1, false, 4, 64>(mw, p, tiles, a.pdl, s);
 }
 
 }  // namespace wqp
