@@ -175,15 +175,11 @@ __device__ __forceinline__ void offset_sums(const uint32_t (&r)[16], int t4, flo
   ns[1] = __shfl_sync(0xFFFFFFFFu, s, 8 * t4 + 4);
 }
 
-// B fragments of one block for one column tile: this thread's 32 activations
-// (row min(g + 8 mt, M - 1), k = kb + 32 t .. + 31) permuted to the code-pair
-// order and pre-scaled, and the offset -2^-69 * sum_k a of the activation rows
-// of its MMA columns.
-__device__ __forceinline__ void build_bfrag(const StreamParams& p, int kb, int mt, int g, int t4, uint32_t (&bf)[16],
-                                            float (&ns)[2]) {
+// This thread's 32 activations of a block for one column tile: row
+// min(g + 8 mt, M - 1), k = kb + 32 t .. + 31.
+__device__ __forceinline__ void load_bact(const StreamParams& p, int kb, int mt, int g, int t4, uint32_t (&r)[16]) {
   const int m = min(g + 8 * mt, p.M - 1);         // rows past M: any valid row, results unused
   const uint16_t* src = p.A + static_cast<size_t>(m) * p.lda + kb + 32 * t4;
-  uint32_t r[16];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint4 v = ld_nc_v4(src + 8 * q);
@@ -192,6 +188,12 @@ __device__ __forceinline__ void build_bfrag(const StreamParams& p, int kb, int m
     r[4 * q + 2] = v.z;
     r[4 * q + 3] = v.w;
   }
+}
+
+// B fragments of one block for one column tile from this thread's 32
+// activations r: permuted to the code-pair order and pre-scaled, and the
+// offset -2^-69 * sum_k a of the activation rows of its MMA columns.
+__device__ __forceinline__ void bfrag_from(const uint32_t (&r)[16], int t4, uint32_t (&bf)[16], float (&ns)[2]) {
 #pragma unroll
   for (int st = 0; st < 8; ++st) {
     const int x = st & 3, o = 8 * (st >> 2) + (x >> 1);
@@ -200,6 +202,13 @@ __device__ __forceinline__ void build_bfrag(const StreamParams& p, int kb, int m
     bf[2 * st + 1] = mul_bf16x2(__byte_perm(r[o + 2], r[o + 6], sel), prescale(x));
   }
   offset_sums(r, t4, ns);
+}
+
+__device__ __forceinline__ void build_bfrag(const StreamParams& p, int kb, int mt, int g, int t4, uint32_t (&bf)[16],
+                                            float (&ns)[2]) {
+  uint32_t r[16];
+  load_bact(p, kb, mt, g, t4, r);
+  bfrag_from(r, t4, bf, ns);
 }
 
 // MT: column tiles of 8 activation rows (1: M <= 8, 2: M <= 16).
@@ -380,15 +389,27 @@ __global__ void __launch_bounds__(threads_for(kOcc), kOcc)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) build_bfrag(p, (st0 * kBlocks + b) * 128, mt, g, t4, bf[mt], ns[mt]);
     } else {
-      // One set per stage of the rank and block, written by the block's
-      // first warp and read by the block's warps (paired CTAs: stage j's set
-      // lives in CTA j % 2 of the pair, at index j / 2).
-      for (int j = 0; j < nst && rq == 0; ++j) {
-        if (pair && (j & 1) != prk) continue;
+      // One set per stage of the rank and block, read by the block's warps
+      // (paired CTAs: stage j's set lives in CTA j % 2 of the pair, at index
+      // j / 2). The block's warps take turns over its stages; each loads the
+      // activations of its next set while it converts the current one.
+      constexpr int kWPB = kCW / kBlocks;         // warps per block
+      const int jstep = pair ? 2 * kWPB : kWPB;
+      const int jfirst = (pair ? prk : 0) + (pair ? 2 : 1) * rq;
+      uint32_t rn[16];
+      if (jfirst < nst) load_bact(p, ((st0 + jfirst) * kBlocks + b) * 128, 0, g, t4, rn);
+      for (int j = jfirst; j < nst; j += jstep) {
         const int jl = pair ? (j >> 1) : j;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          build_bfrag(p, ((st0 + j) * kBlocks + b) * 128, mt, g, t4, bf[mt], ns[mt]);
+          uint32_t rc[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) rc[i] = rn[i];
+          if (mt + 1 < MT)
+            load_bact(p, ((st0 + j) * kBlocks + b) * 128, mt + 1, g, t4, rn);
+          else if (j + jstep < nst)
+            load_bact(p, ((st0 + j + jstep) * kBlocks + b) * 128, 0, g, t4, rn);
+          bfrag_from(rc, t4, bf[mt], ns[mt]);
           const int set = (jl * kBlocks + b) * MT + mt;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
