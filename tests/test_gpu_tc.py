@@ -203,6 +203,16 @@ def test_q2_mma_tall_tiles_ragged(oracle_lib):
         assert np.array_equal(one[0], c8[m]), m
 
 
+def test_q2_mma_tile_height_keeps_rows():
+    """The tile height changes no row's summation order: rows of a call run
+    on 96-row CTAs (N = 7000) equal the same rows of the same weights run on
+    64-row CTAs (N = 5120, the first 5120 rows), bit for bit."""
+    d = G.make("q2", 8, 7000, 5120, seed=35)
+    c96 = G.host_bits(G.run_gpu(d, tc="mma"))
+    c64 = G.host_bits(G.run_gpu(dict(d, N=5120), tc="mma"))
+    assert np.array_equal(c64, c96[:, :5120])
+
+
 def test_q2_mma_paired_ragged(oracle_lib):
     """A ragged shape on the persistent kernel's paired 16-row plan (no K
     split, B fragments shared by two CTAs): N = 20001 leaves a partial last
@@ -486,7 +496,8 @@ def test_f16_mma_rows_independent_and_k_rule(fmt, N):
 
 
 @pytest.mark.parametrize("fmt,N,K,Ms", [("w8", 17408, 5120, (1, 8, 16)), ("w8", 5120, 17408, (2, 16)),
-                                        ("w4", 5120, 5120, (1, 8, 16)), ("w4", 17408, 5120, (4,))])
+                                        ("w8", 17000, 5120, (16,)), ("w4", 5120, 5120, (1, 8, 16)),
+                                        ("w4", 17408, 5120, (4, 16))])
 def test_f16_mma_full_size(oracle_lib, fmt, N, K, Ms):
     for M in Ms:
         d = G.make(fmt, M, N, K, seed=synth.seed_for(3 if fmt == "w8" else 2, M))

@@ -110,7 +110,10 @@ struct Params {
 
 // MT: column tiles of 8 activation rows (1: M <= 8, 2: M <= 16).
 // kRegB: every rank owns one stage, so the B fragments stay in registers.
-template <class F, int MT, bool kRegB, int kOcc>
+// kRebuild: the B fragments of every stage would not fit shared memory beside
+//           the ring (16 rows, no K split), so each item rebuilds its block's
+//           fragments from the activations in L2 instead of keeping them.
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
 __global__ void __launch_bounds__(kThreads, kOcc)
     f16_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
                       const Params p) {
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, kOcc)
     if constexpr (kRegB) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) build((st0 * kBlocks + b) * 128, mt, bf[mt], fo[mt]);
-    } else {
+    } else if constexpr (!kRebuild) {
       for (int j = 0; j < nst; ++j) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -296,7 +299,12 @@ __global__ void __launch_bounds__(kThreads, kOcc)
     bool live = true;
     int s = 0, ph = 0, j = 0, tl = 0;
     for (int it = 0; it < items; ++it) {
-      if constexpr (!kRegB) {
+      if constexpr (kRebuild) {
+        if (nst > 1 || it == 0) {
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) build(((st0 + j) * kBlocks + b) * 128, mt, bf[mt], fo[mt]);
+        }
+      } else if constexpr (!kRegB) {
         if (nst > 1 || it == 0) {
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
@@ -449,22 +457,22 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 constexpr int kBudget2 = 110 * 1024;   // dynamic shared memory of a 2-CTA-per-SM variant
 constexpr int kBudget1 = 220 * 1024;   // of a 1-CTA-per-SM variant
 
-template <class F, int MT, bool kRegB, int kOcc>
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
 struct Variant {
-  static constexpr auto kernel = f16_stream_kernel<F, MT, kRegB, kOcc>;
+  static constexpr auto kernel = f16_stream_kernel<F, MT, kRegB, kOcc, kRebuild>;
   static constexpr int kBudget = kOcc == 2 ? kBudget2 : kBudget1;
 };
 
-template <class F, int MT, bool kRegB, int kOcc>
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
 cudaError_t set_attrs() {
   static AttrLatch latch;
-  using V = Variant<F, MT, kRegB, kOcc>;
+  using V = Variant<F, MT, kRegB, kOcc, kRebuild>;
   return set_smem_attrs(V::kernel, latch, V::kBudget, true);
 }
 
 // Clusters of s CTAs of a variant resident at once (0 if the query failed).
 // Cached per device.
-template <class F, int MT, bool kRegB, int kOcc>
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
 int cluster_capacity(int s) {
   static std::atomic<int> cache[kMaxDevices][kMaxSplits + 1];
   int dev = 0;
@@ -472,7 +480,7 @@ int cluster_capacity(int s) {
   std::atomic<int>& slot = cache[dev][s];
   int v = slot.load(std::memory_order_relaxed);
   if (v != 0) return v > 0 ? v : 0;
-  using V = Variant<F, MT, kRegB, kOcc>;
+  using V = Variant<F, MT, kRegB, kOcc, kRebuild>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(s);
   cfg.blockDim = dim3(kThreads);
@@ -485,7 +493,7 @@ int cluster_capacity(int s) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (set_attrs<F, MT, kRegB, kOcc>() != cudaSuccess ||
+  if (set_attrs<F, MT, kRegB, kOcc, kRebuild>() != cudaSuccess ||
       cudaOccupancyMaxActiveClusters(&n, V::kernel, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();            // the query's failure is not the caller's error
     n = 0;
@@ -496,6 +504,7 @@ int cluster_capacity(int s) {
 
 struct Plan {
   bool regb = false;
+  bool rebuild = false;
   int occ = 1;
   int splits = 1, clusters = 1, ring = 2;
   int red_off = 0, recv_off = 0, bf_off = 0, fo_off = 0, smem = 0;
@@ -506,7 +515,7 @@ template <class F, int MT>
 void layout(Plan& pl, int stages, int budget) {
   using Z = Sizes<F, MT>;
   const int nsmax = (stages + pl.splits - 1) / pl.splits;
-  const int sets = pl.regb ? 0 : nsmax * kCompute * MT;
+  const int sets = (pl.regb || pl.rebuild) ? 0 : nsmax * kCompute * MT;
   const int fixed = Z::kRed + 2 * (pl.splits - 1) * Z::kSlot + sets * (32 * 64 + 32 * 8);
   pl.ring = std::min(kMaxRing, (budget - fixed) / F::kStageBytes);
   pl.red_off = pl.ring * F::kStageBytes;
@@ -522,16 +531,17 @@ void layout(Plan& pl, int stages, int budget) {
 constexpr double kSmRate[3] = {0.0, 1.0, 1.1};
 constexpr double kSplitTileCost = 0.35;
 
-template <class F, int MT, bool kRegB, int kOcc>
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
 void consider(Plan& best, int splits, int tiles, int stages, int num_sms) {
   Plan pl;
   pl.regb = kRegB;
+  pl.rebuild = kRebuild;
   pl.occ = kOcc;
   pl.splits = splits;
-  layout<F, MT>(pl, stages, Variant<F, MT, kRegB, kOcc>::kBudget);
+  layout<F, MT>(pl, stages, Variant<F, MT, kRegB, kOcc, kRebuild>::kBudget);
   if (pl.ring < 2) return;
   const int nsmax = (stages + splits - 1) / splits;
-  const int cap = cluster_capacity<F, MT, kRegB, kOcc>(splits);
+  const int cap = cluster_capacity<F, MT, kRegB, kOcc, kRebuild>(splits);
   const int clusters = std::min(tiles, cap > 0 ? cap : (kOcc * num_sms) / splits);
   if (clusters < 1) return;
   pl.clusters = clusters;
@@ -558,13 +568,18 @@ Plan choose_plan(int tiles, int stages, int num_sms, int only_splits = 0) {
       consider<F, MT, false, 1>(best, s, tiles, stages, num_sms);
     }
   }
+  // Two column tiles whose fragment sets do not fit: rebuild them per item.
+  if constexpr (MT == 2) {
+    for (int s = 1; s <= kMaxSplits && s < stages && best.cost < 0; ++s)
+      if (only_splits <= 0 || s == only_splits) consider<F, 2, false, 1, true>(best, s, tiles, stages, num_sms);
+  }
   return best;
 }
 
-template <class F, int MT, bool kRegB, int kOcc>
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
 cudaError_t launch_variant(const CUtensorMap& mw, const CUtensorMap& ms, const Params& p, bool pdl, int smem,
                            cudaStream_t s) {
-  cudaError_t e = set_attrs<F, MT, kRegB, kOcc>();
+  cudaError_t e = set_attrs<F, MT, kRegB, kOcc, kRebuild>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.clusters * p.splits);
@@ -585,7 +600,7 @@ cudaError_t launch_variant(const CUtensorMap& mw, const CUtensorMap& ms, const P
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, Variant<F, MT, kRegB, kOcc>::kernel, mw, ms, p);
+  return cudaLaunchKernelEx(&cfg, Variant<F, MT, kRegB, kOcc, kRebuild>::kernel, mw, ms, p);
 }
 
 // Plans cached per (device, format, N, K, M tile).
@@ -674,6 +689,7 @@ cudaError_t launch_fmt(const GemvArgs& a, const CUtensorMap& mw, const CUtensorM
     return launch_variant<F, 1, false, 1>(mw, ms, p, a.pdl, pl.smem, s);
   }
   if (pl.regb) return launch_variant<F, 2, true, 1>(mw, ms, p, a.pdl, pl.smem, s);
+  if (pl.rebuild) return launch_variant<F, 2, false, 1, true>(mw, ms, p, a.pdl, pl.smem, s);
   return launch_variant<F, 2, false, 1>(mw, ms, p, a.pdl, pl.smem, s);
 }
 
