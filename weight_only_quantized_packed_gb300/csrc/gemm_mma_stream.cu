@@ -28,15 +28,15 @@
 //         16-row tiles (W = 8) or two of them (W = 16); after the
 //         grid-dependency wait the MMA B fragments of its blocks are built
 //         once per call (in registers when the rank owns one stage, else in
-//         shared memory by the block's first warp) and then it only decodes
-//         codes and issues MMAs. At the end of a tile it hands its sums to
+//         shared memory, the block's warps taking turns over its stages) and
+//         then it only decodes codes and issues MMAs. At the end of a tile it hands its sums to
 //         the epilogue;
 //   W     producer: TMA of the raw stages (64 rows x 272 bytes) into the ring;
 //   W+1   epilogue: adds the 8 blocks' sums of a tile (block order); ranks >= 1
 //         send the result to rank 0 with st.async (completing on rank 0's
-//         mbarrier), rank 0 adds them in rank order and stores C. A one-slot
-//         receive buffer with a "free" barrier per peer (arrived from rank 0)
-//         paces the peers.
+//         mbarrier), rank 0 adds them in rank order and stores C. A two-slot
+//         receive buffer paces the peers: each peer has a "free" barrier per
+//         slot, on which rank 0 arrives once it has read the slot.
 // Per 128-K block b and thread (g = lane / 4, t = lane % 4):
 //   * A fragment: code words 2t and 2t + 1 of the block, rows g and g + 8 of
 //     a tile. Word bits 2q..2q+1 hold code q (q < 16). The pair of 16-bit
