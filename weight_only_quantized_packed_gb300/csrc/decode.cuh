@@ -14,30 +14,6 @@ namespace wqp {
 // Q2_0 block ("spark_model/layers/ops/gemv_q2_vec.rs", module docs and the
 // test helper `gemv_row`): 34 bytes = 32 bytes of 2-bit codes, code i in bits
 // 2*(i%4) of byte i/4, then the fp16 scale d; weight = ((code & 3) - 1) * d.
-//
-// A 32-bit word q holds codes c0..c15 at bits 2i. Each pair (c_j, c_j+8)
-// sits at bits (2j, 2j+16). OR-ing the masked fields into the mantissa of a
-// BF16 constant 2^e gives 2^e + c exactly when the field's lowest bit has
-// weight 1: 128 + c for bits 0-1, 32 + c for bits 2-3 and 8 + c for bits 4-5.
-// Subtracting 2^e + 1 then leaves c - 1 in {-1, 0, 1, 2}. The result pairs
-// are p[j] = (lo: c_j - 1, hi: c_{j+8} - 1), the J8 layout.
-__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-__device__ __forceinline__ void q2_decode_word(uint32_t q, uint32_t (&p)[8]) {
-  const uint32_t q6 = q >> 6, q12 = q >> 12;
-  p[0] = sub_bf16x2((q & 0x00030003u) | 0x43004300u, 0x43014301u);    // 128+c - 129
-  p[1] = sub_bf16x2((q & 0x000C000Cu) | 0x42004200u, 0x42044204u);    //  32+c -  33
-  p[2] = sub_bf16x2((q & 0x00300030u) | 0x41004100u, 0x41104110u);    //   8+c -   9
-  p[3] = sub_bf16x2((q6 & 0x00030003u) | 0x43004300u, 0x43014301u);
-  p[4] = sub_bf16x2((q6 & 0x000C000Cu) | 0x42004200u, 0x42044204u);
-  p[5] = sub_bf16x2((q6 & 0x00300030u) | 0x41004100u, 0x41104110u);
-  p[6] = sub_bf16x2((q12 & 0x00030003u) | 0x43004300u, 0x43014301u);
-  p[7] = sub_bf16x2((q12 & 0x000C000Cu) | 0x42004200u, 0x42044204u);
-}
 
 // Position factor of code j of a 16-code word: 4^j for j <= 10, 4^(j - 11)
 // for j >= 11 (those fields are shifted down by 22 bits before masking).
@@ -74,14 +50,6 @@ __device__ __forceinline__ float q2_scale(const uint8_t* blk) {
 }
 
 // ---------------------------------------------------------------- FP8 / FP4
-// f16x2 -> bf16x2 for values that are exactly representable in both.
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
-  const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
-  const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&b);
-}
-
 // Two E4M3 codes (low byte = first element) -> f16x2 (exact: E4M3 is a subset
 // of binary16; NaN stays NaN).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
@@ -125,12 +93,6 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2_exact(uint32_t h) {
 __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t x, uint32_t& p01, uint32_t& p23) {
   p01 = f16x2_to_bf16x2_exact(e4m3x2_to_f16x2(x & 0xFFFFu));
   p23 = f16x2_to_bf16x2_exact(e4m3x2_to_f16x2(x >> 16));
-}
-
-// Four bytes = eight E2M1 codes of word x -> four bf16x2 pairs in element order.
-__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t x, uint32_t* p) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = f16x2_to_bf16x2(e2m1x2_to_f16x2((x >> (8 * i)) & 0xFFu));
 }
 
 }  // namespace wqp
