@@ -407,7 +407,7 @@ F16_FMTS = pytest.mark.parametrize("fmt", ["w8", "w4"])
 @F16_FMTS
 @pytest.mark.parametrize("N,K", [(128, 1024), (200, 2048), (1000, 1024), (77, 3072), (384, 8192)])
 def test_f16_mma_parity_small(oracle_lib, fmt, N, K):
-    for M in (1, 5, 8, 16):
+    for M in (1, 5, 7, 8, 16):
         d = G.make(fmt, M, N, K, seed=1300 + N + K + M)
         C = G.host_bits(G.run_gpu(d, tc="mma"))
         _check_tc(oracle_lib, d, C, f"{fmt} mma M={M} N={N} K={K}")
