@@ -22,8 +22,8 @@
 // tile. Clusters are persistent: cluster c handles tiles c, c + C, c + 2C, ...
 // and each CTA streams its (tile, stage) items through a ring of raw stages.
 //
-// Warps of a CTA (W = 8 compute warps when several CTAs share an SM, 16
-// when one CTA has the SM):
+// Warps of a CTA (W = 16 compute warps when one CTA has the SM and the
+// launch has one 8-row column tile, else 8):
 //   0..W-1 compute: warp w owns block w % 8 of every stage, for all four
 //         16-row tiles (W = 8) or two of them (W = 16); after the
 //         grid-dependency wait the MMA B fragments of its blocks are built
@@ -71,10 +71,13 @@ namespace mmas {
 constexpr int BM = 64;                       // weight rows per tile
 constexpr int kTiles = 4;                    // 16-row MMA tiles per tile
 // Compute warps: one per 128-K block of a stage and all four row tiles when
-// several CTAs share an SM; with one CTA per SM two per block, each with two
-// of the row tiles (more warps to hide the mask -> MMA latencies).
-constexpr int compute_warps(int occ) { return occ == 1 ? 16 : 8; }
-constexpr int threads_for(int occ) { return (compute_warps(occ) + 2) * 32; }
+// several CTAs share an SM or the launch has two column tiles (each warp's
+// four row tiles against both keep enough MMA chains in flight: gate+up at
+// M = 16 34.4 -> 31.6 us against 16 warps); with one CTA per SM and one
+// column tile two per block, each with two of the row tiles (more warps to
+// hide the mask -> MMA latencies).
+constexpr int compute_warps(int occ, int mt) { return occ == 1 && mt == 1 ? 16 : 8; }
+constexpr int threads_for(int occ, int mt) { return (compute_warps(occ, mt) + 2) * 32; }
 constexpr int kBlocks = 8;                   // 128-K blocks per raw stage (1024 K)
 constexpr int kRowBytes = kBlocks * 34;      // 272: 17 x 16 bytes
 constexpr int kStageBytes = BM * kRowBytes;  // 17408
@@ -220,10 +223,10 @@ __device__ __forceinline__ void build_bfrag(const StreamParams& p, int kb, int m
 //        sets (each stores those of every other stage), for 16-row calls
 //        whose sets would not fit one CTA.
 template <int MT, bool kRegB, int kOcc, bool kPair = false>
-__global__ void __launch_bounds__(threads_for(kOcc), kOcc)
+__global__ void __launch_bounds__(threads_for(kOcc, MT), kOcc)
     q2_stream_kernel(const __grid_constant__ CUtensorMap tmW, const StreamParams p) {
   using Z = Sizes<MT>;
-  constexpr int kCW = compute_warps(kOcc);        // compute warps
+  constexpr int kCW = compute_warps(kOcc, MT);    // compute warps
   constexpr int kTPW = kTiles * kBlocks / kCW;    // row tiles per compute warp (4 or 2)
   constexpr int kProducer = kCW;                  // warp index of the TMA producer
   constexpr int kEpilogue = kCW + 1;              // warp index of the epilogue
@@ -607,7 +610,7 @@ int cluster_capacity(int s) {
   using V = Variant<MT, kRegB, kOcc, kPair>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(s);
-  cfg.blockDim = dim3(threads_for(kOcc));
+  cfg.blockDim = dim3(threads_for(kOcc, MT));
   cfg.dynamicSmemBytes = V::kBudget;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -742,7 +745,7 @@ cudaError_t launch_variant(const CUtensorMap& mw, const StreamParams& p, bool pd
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.clusters * p.splits);
-  cfg.blockDim = dim3(threads_for(kOcc));
+  cfg.blockDim = dim3(threads_for(kOcc, MT));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
