@@ -189,6 +189,22 @@ def test_q2_mma_persistent_rows_independent():
         assert np.array_equal(one[0], c16[m]), m
 
 
+@pytest.mark.parametrize("K", [1024, 2048])
+def test_q2_mma_persistent_register_fragments(oracle_lib, K):
+    """Persistent plans whose ranks own one stage each (B fragments kept in
+    registers): N = 20000 (persistent, a ragged last tile) at K = 1024 and
+    2048, 5 and 16 rows; parity with the oracle and rows equal to the rows
+    computed alone."""
+    N = 20000
+    for M in (5, 16):
+        d = G.make("q2", M, N, K, seed=37 + M + K)
+        C = G.host_bits(G.run_gpu(d, tc="mma"))
+        _check_tc(oracle_lib, d, C, f"q2 persistent M={M} N={N} K={K} mma")
+        for m in (0, M - 1):
+            one = G.host_bits(G.run_gpu(d, tc="mma", A=d["dA"][m:m + 1]))
+            assert np.array_equal(one[0], C[m]), (M, m)
+
+
 def test_q2_mma_tall_tiles_ragged(oracle_lib):
     """A shape whose single-stage grid of 64-row CTAs would need a fourth CTA
     slot per SM runs as 96-row CTAs (N = 7000, K = 5120: a partial last
@@ -497,7 +513,7 @@ def test_f16_mma_rows_independent_and_k_rule(fmt, N):
 
 @pytest.mark.parametrize("fmt,N,K,Ms", [("w8", 17408, 5120, (1, 8, 16)), ("w8", 5120, 17408, (2, 16)),
                                         ("w8", 17000, 5120, (16,)), ("w4", 5120, 5120, (1, 8, 16)),
-                                        ("w4", 17408, 5120, (4, 16))])
+                                        ("w4", 17408, 5120, (4, 16)), ("w4", 20000, 5120, (3, 16))])
 def test_f16_mma_full_size(oracle_lib, fmt, N, K, Ms):
     for M in Ms:
         d = G.make(fmt, M, N, K, seed=synth.seed_for(3 if fmt == "w8" else 2, M))

@@ -714,7 +714,7 @@ cudaError_t launch_w8a16_gemm_mma(const GemvArgs& a, cudaStream_t s) {
 // Requires K % 1024 == 0 (checked by the caller).
 cudaError_t launch_w4a16_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   using namespace mmaf;
-  // Fewer than two 64-row tiles per SM (and at most 8 stages): short CTAs,
+  // Fewer than 1.75 64-row tiles per SM (and at most 8 stages): short CTAs,
   // three per SM, 8 rows per launch. The choice depends on the shape only,
   // so a row's result does not depend on M.
   if (w4a16_short_fits(a)) {

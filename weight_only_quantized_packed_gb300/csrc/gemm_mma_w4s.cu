@@ -273,7 +273,10 @@ cudaError_t set_attrs() {
 
 bool w4a16_short_fits(const GemvArgs& a) {
   const int tiles = (a.N + mmaw4s::BM - 1) / mmaw4s::BM, stages = a.K / 1024;
-  return tiles < 2 * a.num_sms && stages <= mmaw4s::kMaxSplits;
+  // Measured (5120-K shapes): short CTAs win up to 192 tiles (N = 12288:
+  // 10.8 / 12.3 us at M = 1 / 8 against 13.8 / 14.5 persistent), the
+  // persistent kernel from 272 (N = 17408: 13.6 / 15.2 against 14.1 / 15.7).
+  return 4 * tiles < 7 * a.num_sms && stages <= mmaw4s::kMaxSplits;
 }
 
 // Requires K % 1024 == 0, K / 1024 <= 8 and M <= 8 (checked by the caller).
