@@ -161,8 +161,12 @@ int w4a16_gemm_tc_ex(const void* A, int lda, const void* W, const void* scales,
 
 /* Warp-level tensor-core form of w4a16_gemv (mma.sync m16n8k16, FP16
  * operands, FP32 accumulation), swap-AB with 16 weight rows by 8 activation
- * rows per MMA (two column tiles for M = 9..16, so the weights are read once
- * for up to 16 rows). The weight operand is e2m1 * e4m3(scale), exact in
+ * rows per MMA. Shapes of at least 1.75 64-row tiles per SM, or of more than
+ * 8 K stages of 1024, run on a persistent kernel with two column tiles for
+ * M = 9..16, so the weights are read once for up to 16 rows; smaller shapes
+ * run one short CTA per (tile, K stage) and 8 rows per launch (M = 9..16 is
+ * two launches). The choice depends on N and K only, never on M. The weight
+ * operand is e2m1 * e4m3(scale), exact in
  * FP16. Each activation row is scaled per 128-K block by the power of two
  * 2^e that puts its largest magnitude in [2^14, 2^15) and rounded to FP16
  * (exact for every value of at least 2^-31 times that maximum); each block's
