@@ -113,11 +113,15 @@ struct Params {
 // kRebuild: the B fragments of every stage would not fit shared memory beside
 //           the ring (16 rows, no K split), so each item rebuilds its block's
 //           fragments from the activations in L2 instead of keeping them.
-template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
+// kNS: a rank owns at most kNS stages and each warp keeps its block's B
+//      fragments of all of them in registers (8 rows, one CTA per SM), which
+//      leaves the shared memory to the ring.
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false, int kNS = 0>
 __global__ void __launch_bounds__(kThreads, kOcc)
     f16_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
                       const Params p) {
   using Z = Sizes<F, MT>;
+  static_assert(kNS == 0 || (MT == 1 && !kRegB && !kRebuild), "register-held fragment sets: 8 rows");
   constexpr int BM = F::BM, kTiles = F::kTiles;
   extern __shared__ __align__(1024) uint8_t smem[];
   // full[R], empty[R], red_full, red_empty, recv_full[2], recv_free[2]
@@ -271,7 +275,13 @@ __global__ void __launch_bounds__(kThreads, kOcc)
       f[0] = __shfl_sync(0xFFFFFFFFu, inv, 8 * t4);
       f[1] = __shfl_sync(0xFFFFFFFFu, inv, 8 * t4 + 4);
     };
-    if constexpr (kRegB) {
+    uint32_t bfa[kNS > 0 ? kNS : 1][MT][16];      // kNS: every stage's fragments
+    float foa[kNS > 0 ? kNS : 1][MT][2];
+    if constexpr (kNS > 0) {
+#pragma unroll
+      for (int js = 0; js < kNS; ++js)
+        if (js < nst) build(((st0 + js) * kBlocks + b) * 128, 0, bfa[js][0], foa[js][0]);
+    } else if constexpr (kRegB) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) build((st0 * kBlocks + b) * 128, mt, bf[mt], fo[mt]);
     } else if constexpr (!kRebuild) {
@@ -298,31 +308,8 @@ __global__ void __launch_bounds__(kThreads, kOcc)
     float4* red = reinterpret_cast<float4*>(smem + p.red_off) + warp * Z::kItems;
     bool live = true;
     int s = 0, ph = 0, j = 0, tl = 0;
-    for (int it = 0; it < items; ++it) {
-      if constexpr (kRebuild) {
-        if (nst > 1 || it == 0) {
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) build(((st0 + j) * kBlocks + b) * 128, mt, bf[mt], fo[mt]);
-        }
-      } else if constexpr (!kRegB) {
-        if (nst > 1 || it == 0) {
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const int set = (j * kCompute + b) * MT + mt;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint4 u = bfs[(set * 4 + q) * 32 + lane];
-              bf[mt][4 * q] = u.x;
-              bf[mt][4 * q + 1] = u.y;
-              bf[mt][4 * q + 2] = u.z;
-              bf[mt][4 * q + 3] = u.w;
-            }
-            const float2 f2 = fos[set * 32 + lane];
-            fo[mt][0] = f2.x;
-            fo[mt][1] = f2.y;
-          }
-        }
-      }
+    // One (tile, stage) item against the stage's fragments bfx / fox.
+    auto item = [&](const uint32_t (&bfx)[MT][16], const float (&fox)[MT][2]) {
       if (live) live = tc::wait_or_abort(full0 + 8 * s, ph, p.err, abort_flag);
       live = __all_sync(0xFFFFFFFFu, live);
       if (live) {
@@ -334,12 +321,12 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           if constexpr (F::kW4) {
-            f[mt][0] = fo[mt][0];
-            f[mt][1] = fo[mt][1];
+            f[mt][0] = fox[mt][0];
+            f[mt][1] = fox[mt][1];
           } else {
             const float sb = reinterpret_cast<const float*>(stage + F::kScaleOff)[b];
-            f[mt][0] = sb * fo[mt][0];
-            f[mt][1] = sb * fo[mt][1];
+            f[mt][0] = sb * fox[mt][0];
+            f[mt][1] = sb * fox[mt][1];
           }
         }
 #pragma unroll
@@ -403,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
                 if (jj == 0)
-                  mma_f16_16816_z(c[i][mt], a0, a1, a2, a3, bf[mt][0], bf[mt][1]);
+                  mma_f16_16816_z(c[i][mt], a0, a1, a2, a3, bfx[mt][0], bfx[mt][1]);
                 else
-                  mma_f16_16816(c[i][mt], a0, a1, a2, a3, bf[mt][2 * jj], bf[mt][2 * jj + 1]);
+                  mma_f16_16816(c[i][mt], a0, a1, a2, a3, bfx[mt][2 * jj], bfx[mt][2 * jj + 1]);
               }
             }
           }
@@ -445,6 +432,41 @@ __global__ void __launch_bounds__(kThreads, kOcc)
         if (lane == 0) mbar_arrive(red_full);
         ++tl;
       }
+    };
+    if constexpr (kNS > 0) {
+      for (int ti = 0; ti < ntile; ++ti) {
+#pragma unroll
+        for (int js = 0; js < kNS; ++js)
+          if (js < nst) item(bfa[js], foa[js]);
+      }
+    } else {
+      for (int it = 0; it < items; ++it) {
+        if constexpr (kRebuild) {
+          if (nst > 1 || it == 0) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) build(((st0 + j) * kBlocks + b) * 128, mt, bf[mt], fo[mt]);
+          }
+        } else if constexpr (!kRegB) {
+          if (nst > 1 || it == 0) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              const int set = (j * kCompute + b) * MT + mt;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 u = bfs[(set * 4 + q) * 32 + lane];
+                bf[mt][4 * q] = u.x;
+                bf[mt][4 * q + 1] = u.y;
+                bf[mt][4 * q + 2] = u.z;
+                bf[mt][4 * q + 3] = u.w;
+              }
+              const float2 f2 = fos[set * 32 + lane];
+              fo[mt][0] = f2.x;
+              fo[mt][1] = f2.y;
+            }
+          }
+        }
+        item(bf, fo);
+      }
     }
   }
   // Every CTA of the cluster stays until all are done: peers' st.async into
@@ -454,19 +476,20 @@ __global__ void __launch_bounds__(kThreads, kOcc)
 }
 
 // ---------------------------------------------------------------- host side
+constexpr int kMaxRegSets = 5;        // stages per rank whose fragment sets fit in registers
 constexpr int kBudget2 = 110 * 1024;   // dynamic shared memory of a 2-CTA-per-SM variant
 constexpr int kBudget1 = 220 * 1024;   // of a 1-CTA-per-SM variant
 
-template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false, int kNS = 0>
 struct Variant {
-  static constexpr auto kernel = f16_stream_kernel<F, MT, kRegB, kOcc, kRebuild>;
+  static constexpr auto kernel = f16_stream_kernel<F, MT, kRegB, kOcc, kRebuild, kNS>;
   static constexpr int kBudget = kOcc == 2 ? kBudget2 : kBudget1;
 };
 
-template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false, int kNS = 0>
 cudaError_t set_attrs() {
   static AttrLatch latch;
-  using V = Variant<F, MT, kRegB, kOcc, kRebuild>;
+  using V = Variant<F, MT, kRegB, kOcc, kRebuild, kNS>;
   return set_smem_attrs(V::kernel, latch, V::kBudget, true);
 }
 
@@ -505,6 +528,7 @@ int cluster_capacity(int s) {
 struct Plan {
   bool regb = false;
   bool rebuild = false;
+  int ns = 0;          // > 0: each warp keeps the fragments of its ns stages in registers
   int occ = 1;
   int splits = 1, clusters = 1, ring = 2;
   int red_off = 0, recv_off = 0, bf_off = 0, fo_off = 0, smem = 0;
@@ -515,7 +539,7 @@ template <class F, int MT>
 void layout(Plan& pl, int stages, int budget) {
   using Z = Sizes<F, MT>;
   const int nsmax = (stages + pl.splits - 1) / pl.splits;
-  const int sets = (pl.regb || pl.rebuild) ? 0 : nsmax * kCompute * MT;
+  const int sets = (pl.regb || pl.rebuild || pl.ns > 0) ? 0 : nsmax * kCompute * MT;
   const int fixed = Z::kRed + 2 * (pl.splits - 1) * Z::kSlot + sets * (32 * 64 + 32 * 8);
   pl.ring = std::min(kMaxRing, (budget - fixed) / F::kStageBytes);
   pl.red_off = pl.ring * F::kStageBytes;
@@ -576,10 +600,10 @@ Plan choose_plan(int tiles, int stages, int num_sms, int only_splits = 0) {
   return best;
 }
 
-template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false>
+template <class F, int MT, bool kRegB, int kOcc, bool kRebuild = false, int kNS = 0>
 cudaError_t launch_variant(const CUtensorMap& mw, const CUtensorMap& ms, const Params& p, bool pdl, int smem,
                            cudaStream_t s) {
-  cudaError_t e = set_attrs<F, MT, kRegB, kOcc, kRebuild>();
+  cudaError_t e = set_attrs<F, MT, kRegB, kOcc, kRebuild, kNS>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.clusters * p.splits);
@@ -600,7 +624,7 @@ cudaError_t launch_variant(const CUtensorMap& mw, const CUtensorMap& ms, const P
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, Variant<F, MT, kRegB, kOcc, kRebuild>::kernel, mw, ms, p);
+  return cudaLaunchKernelEx(&cfg, Variant<F, MT, kRegB, kOcc, kRebuild, kNS>::kernel, mw, ms, p);
 }
 
 // Plans cached per (device, format, N, K, M tile).
@@ -686,6 +710,29 @@ cudaError_t launch_fmt(const GemvArgs& a, const CUtensorMap& mw, const CUtensorM
   if (mt == 1) {
     if (pl.regb) return pl.occ == 2 ? launch_variant<F, 1, true, 2>(mw, ms, p, a.pdl, pl.smem, s)
                                     : launch_variant<F, 1, true, 1>(mw, ms, p, a.pdl, pl.smem, s);
+    // FP8, a rank of at most kMaxRegSets stages: its fragment sets in
+    // registers, the shared memory they would take to the ring (17408 x 5120:
+    // 3 -> 6 raw stages in flight, 17.8 -> 15.8 us at M = 1). W4 measured
+    // slower this way (13.6 -> 14.0 us at 17408 x 5120).
+    if constexpr (!F::kW4) {
+      const int nsmax = (stages + pl.splits - 1) / pl.splits;
+      if (nsmax >= 2 && nsmax <= kMaxRegSets) {
+        Plan pr = pl;
+        pr.ns = nsmax;
+        layout<F, 1>(pr, stages, kBudget1);
+        p.ring = pr.ring;
+        p.red_off = pr.red_off;
+        p.recv_off = pr.recv_off;
+        p.bf_off = pr.bf_off;
+        p.fo_off = pr.fo_off;
+        switch (nsmax) {
+          case 2: return launch_variant<F, 1, false, 1, false, 2>(mw, ms, p, a.pdl, pr.smem, s);
+          case 3: return launch_variant<F, 1, false, 1, false, 3>(mw, ms, p, a.pdl, pr.smem, s);
+          case 4: return launch_variant<F, 1, false, 1, false, 4>(mw, ms, p, a.pdl, pr.smem, s);
+          default: return launch_variant<F, 1, false, 1, false, 5>(mw, ms, p, a.pdl, pr.smem, s);
+        }
+      }
+    }
     return launch_variant<F, 1, false, 1>(mw, ms, p, a.pdl, pl.smem, s);
   }
   if (pl.regb) return launch_variant<F, 2, true, 1>(mw, ms, p, a.pdl, pl.smem, s);
