@@ -106,13 +106,13 @@ int q2_gemm_tc_strided(const void* A, int lda, const void* W, void* C, int ldc,
  * cluster and the partial sums are added in rank order in shared memory.
  * Arguments, layouts and limits are those of q2_gemm_tc (K % 1024 == 0,
  * |a| < 2^62); anything else gives WQP_ERR_INVALID_ARG.
- * Shapes of at least two 64-row tiles per SM (N >= 128 * SMs) run on a
- * persistent kernel whose CTAs build their activation fragments once and
- * stream their weight tiles through a ring of raw stages; one launch serves
- * up to 16 activation rows (two column tiles), so the weights are read once
- * for all of them. Smaller shapes run one short CTA per (tile, K range) and
- * 8 activation rows per launch (M = 9..16 is two launches). The choice
- * depends on N only, never on M.
+ * Shapes of at least two 64-row tiles per SM (N >= 128 * SMs) with
+ * K <= 57344 run on a persistent kernel whose CTAs build their activation
+ * fragments once and stream their weight tiles through a ring of raw
+ * stages; one launch serves up to 16 activation rows (two column tiles), so
+ * the weights are read once for all of them. Other shapes run one short CTA
+ * per (tile, K range) and 8 activation rows per launch (M = 9..16 is two
+ * launches). The choice depends on N and K only, never on M.
  * Numerics: the scalar contract of q2_gemm_tc. Not bit-identical to q2_gemv
  * or q2_gemm_tc. A row does not depend on the other rows of the call.
  * Device-side waits are bounded as for the other kernels (see

@@ -539,3 +539,63 @@ def test_f16_mma_m_above_16(oracle_lib, fmt):
         for m in (0, 16, M - 1):
             one = G.host_bits(G.run_gpu(d, tc="mma", A=d["dA"][m:m + 1]))
             assert np.array_equal(one[0], C[m]), (M, m)
+
+
+# -------------------------------------------------------------------- long K
+# The persistent kernels keep each rank's B-fragment sets in shared memory
+# beside a ring of two stages; at 8 K splits those fit up to K = 57344 for
+# Q2_0 and FP8 and K = 43008 for W4. Past that, Q2_0 runs on the short-CTA
+# kernel and FP8 / W4 rebuild each item's fragments. The weights are a seeded
+# block of R rows repeated down N, and the oracle runs on the block.
+def _tiled(fmt, M, N, K, R, seed):
+    base = G.make(fmt, M, R, K, seed=seed)
+    reps = -(-N // R)
+    W = np.tile(base["W"], (reps, 1))[:N]
+    d = dict(base, N=N, W=W, dW=G.dev_u8(W))
+    if fmt == "w4":
+        S = np.tile(base["S"], (reps, 1))[:N]
+        d.update(S=S, dS=G.dev_u8(S))
+    elif fmt == "w8":
+        assert R % 128 == 0                      # whole 128-row scale groups
+        S = np.tile(base["S"], (reps, 1))[:-(-N // 128)]
+        d.update(S=S, dS=G.dev_f32(S))
+    return base, d
+
+
+def _tiled_ref(ref, N):
+    reps = -(-N // ref.c.shape[1])
+    return type(ref)(np.tile(ref.c, (1, reps))[:, :N], np.tile(ref.r, (1, reps))[:, :N],
+                     np.tile(ref.s, (1, reps))[:, :N])
+
+
+@pytest.mark.parametrize("fmt", ["q2", "w8", "w4"])
+def test_mma_long_k(oracle_lib, fmt):
+    """K = 65536 on the warp-level MMA engines, past the fragment-set limit.
+    Q2_0 at N = 128 x SMs + 37, a shape the persistent kernel takes at a
+    shorter K; FP8 and W4 at a ragged N = 4133. 16 rows against the oracle
+    on every output, and the first 3 rows equal to a 3-row call's."""
+    import torch
+
+    K, R = 65536, 256
+    N = 128 * torch.cuda.get_device_properties(0).multi_processor_count + 37 if fmt == "q2" else 4133
+    base, d = _tiled(fmt, 16, N, K, R, seed=970)
+    ref = _tiled_ref(G.run_oracle(oracle_lib, base), N)
+    C16 = G.host_bits(G.run_gpu(d, tc="mma"))
+    assert_scalar_term(C16, ref, K, f"{fmt} mma long K M=16 N={N} K={K}")
+    C3 = G.host_bits(G.run_gpu(d, tc="mma", A=d["dA"][:3]))
+    assert np.array_equal(C3, C16[:3])
+
+
+@pytest.mark.parametrize("fmt", ["q2", "w8", "w4"])
+def test_largest_k_every_engine(oracle_lib, fmt):
+    """K = 2^20, the largest K the C ABI accepts, on the scalar, tcgen05 and
+    warp-level MMA engines of each format (N = 40, M = 3): the scalar term
+    (the FP8 tensor-core term on tcgen05) against the oracle."""
+    K, N, M = 1 << 20, 40, 3
+    d = G.make(fmt, M, N, K, seed=980)
+    ref = G.run_oracle(oracle_lib, d)
+    C = G.host_bits(G.run_gpu(d))
+    assert_scalar_term(C, ref, K, f"{fmt} scalar K={K}")
+    for eng in (True, "mma"):
+        C = G.host_bits(G.run_gpu(d, tc=eng))
+        _check_tc(oracle_lib, d, C, f"{fmt} {eng} K={K}")

@@ -598,10 +598,11 @@ cudaError_t launch_variant(const CUtensorMap& mw, const MmaParams& p, int tiles,
 cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s) {
   using namespace mma;
   // At least two 64-row tiles per SM: the persistent kernel (weights read once
-  // for up to 16 rows; B fragments built once per CTA). Otherwise one short
-  // CTA per (tile, stage range) and 8 activation rows per launch. The choice
-  // depends on the shape only, so a row's result does not depend on M.
-  if ((a.N + 63) / 64 >= 2 * a.num_sms) return launch_q2_gemm_stream(a, s);
+  // for up to 16 rows; B fragments built once per CTA), where its plan fits
+  // (K <= 57344). Otherwise one short CTA per (tile, stage range) and 8
+  // activation rows per launch. The choice depends on the shape only, so a
+  // row's result does not depend on M.
+  if ((a.N + 63) / 64 >= 2 * a.num_sms && q2_gemm_stream_fits(a)) return launch_q2_gemm_stream(a, s);
   if (a.M > 8) {
     GemvArgs lo = a, hi = a;
     lo.M = 8;

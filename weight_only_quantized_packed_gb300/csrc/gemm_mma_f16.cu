@@ -111,8 +111,9 @@ struct Params {
 // MT: column tiles of 8 activation rows (1: M <= 8, 2: M <= 16).
 // kRegB: every rank owns one stage, so the B fragments stay in registers.
 // kRebuild: the B fragments of every stage would not fit shared memory beside
-//           the ring (16 rows, no K split), so each item rebuilds its block's
-//           fragments from the activations in L2 instead of keeping them.
+//           the ring (16 rows with no K split, or a long K), so each item
+//           rebuilds its block's fragments from the activations in L2 instead
+//           of keeping them.
 // kNS: a rank owns at most kNS stages and each warp keeps its block's B
 //      fragments of all of them in registers (8 rows, one CTA per SM), which
 //      leaves the shared memory to the ring.
@@ -592,10 +593,12 @@ Plan choose_plan(int tiles, int stages, int num_sms, int only_splits = 0) {
       consider<F, MT, false, 1>(best, s, tiles, stages, num_sms);
     }
   }
-  // Two column tiles whose fragment sets do not fit: rebuild them per item.
-  if constexpr (MT == 2) {
-    for (int s = 1; s <= kMaxSplits && s < stages && best.cost < 0; ++s)
-      if (only_splits <= 0 || s == only_splits) consider<F, 2, false, 1, true>(best, s, tiles, stages, num_sms);
+  // Fragment sets that do not fit beside a ring of two stages (two column
+  // tiles with no K split; any M tile past K = 57344 for FP8 and K = 43008
+  // for W4 at 8 splits): each item rebuilds its block's fragments instead.
+  if (best.cost < 0) {
+    for (int s = 1; s <= kMaxSplits && s < stages; ++s)
+      if (only_splits <= 0 || s == only_splits) consider<F, MT, false, 1, true>(best, s, tiles, stages, num_sms);
   }
   return best;
 }
@@ -710,6 +713,7 @@ cudaError_t launch_fmt(const GemvArgs& a, const CUtensorMap& mw, const CUtensorM
   if (mt == 1) {
     if (pl.regb) return pl.occ == 2 ? launch_variant<F, 1, true, 2>(mw, ms, p, a.pdl, pl.smem, s)
                                     : launch_variant<F, 1, true, 1>(mw, ms, p, a.pdl, pl.smem, s);
+    if (pl.rebuild) return launch_variant<F, 1, false, 1, true>(mw, ms, p, a.pdl, pl.smem, s);
     // FP8, a rank of at most kMaxRegSets stages: its fragment sets in
     // registers, the shared memory they would take to the ring (17408 x 5120:
     // 3 -> 6 raw stages in flight, 17.8 -> 15.8 us at M = 1). W4 measured

@@ -767,39 +767,54 @@ cudaError_t launch_variant(const CUtensorMap& mw, const StreamParams& p, bool pd
 
 }  // namespace mmas
 
+namespace mmas {
+// The plan of a shape and M tile on the current device, cached. The K split
+// (and so every row's summation order) is the one of the 8-row plan for
+// every M, so a row's result does not depend on how many rows the call has.
+cudaError_t plan_for(const GemvArgs& a, int mt, Plan& pl) {
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.N + BM - 1) / BM, stages = a.K / (kBlocks * 128);
+  const PlanKey key{dev, a.N, a.K, mt};
+  PlanCache& pc = plan_cache();
+  {
+    std::lock_guard<std::mutex> lk(pc.mu);
+    for (int i = 0; i < pc.n; ++i)
+      if (pc.key[i] == key) {
+        pl = pc.plan[i];
+        return cudaSuccess;
+      }
+  }
+  pl = choose_plan<1>(tiles, stages, a.num_sms);
+  if (pl.cost >= 0 && mt == 2) pl = choose_plan<2>(tiles, stages, a.num_sms, pl.splits);
+  std::lock_guard<std::mutex> lk(pc.mu);
+  const int i = pc.n < kPlanCache ? pc.n++ : (pc.next++ % kPlanCache);
+  pc.key[i] = key;
+  pc.plan[i] = pl;
+  return cudaSuccess;
+}
+}  // namespace mmas
+
+// An 8-row plan needs a rank's B-fragment sets (18 KB per stage) and a ring
+// of two stages in one CTA's shared memory: with 8 K splits, up to 7 stages
+// per rank (K <= 57344). Longer K runs on the short-CTA kernel. The answer
+// depends on N, K and the device only.
+bool q2_gemm_stream_fits(const GemvArgs& a) {
+  mmas::Plan pl;
+  return mmas::plan_for(a, 1, pl) == cudaSuccess && pl.cost >= 0;
+}
+
 // Requires K % 1024 == 0 (checked by the caller): a row is then 34 * K / 128
 // bytes, a multiple of 16, and each raw stage of 8 blocks starts on a 16-byte
 // boundary (the TMA box's x = 136 * stage elements of 2 bytes).
 cudaError_t launch_q2_gemm_stream(const GemvArgs& a, cudaStream_t s) {
   using namespace mmas;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
   const int mt = a.M > 8 ? 2 : 1;
   const int tiles = (a.N + BM - 1) / BM, stages = a.K / (kBlocks * 128);
-  const PlanKey key{dev, a.N, a.K, mt};
   Plan pl;
-  bool have = false;
-  PlanCache& pc = plan_cache();
-  {
-    std::lock_guard<std::mutex> lk(pc.mu);
-    for (int i = 0; i < pc.n && !have; ++i)
-      if (pc.key[i] == key) {
-        pl = pc.plan[i];
-        have = true;
-      }
-  }
-  if (!have) {
-    // The K split (and so every row's summation order) is the one of the
-    // 8-row plan for every M, so a row's result does not depend on how many
-    // rows the call has.
-    pl = choose_plan<1>(tiles, stages, a.num_sms);
-    if (pl.cost >= 0 && mt == 2) pl = choose_plan<2>(tiles, stages, a.num_sms, pl.splits);
-    std::lock_guard<std::mutex> lk(pc.mu);
-    const int i = pc.n < kPlanCache ? pc.n++ : (pc.next++ % kPlanCache);
-    pc.key[i] = key;
-    pc.plan[i] = pl;
-  }
+  cudaError_t e = plan_for(a, mt, pl);
+  if (e != cudaSuccess) return e;
   if (pl.cost < 0) {
     if (mt == 1) return cudaErrorInvalidConfiguration;
     // No two-column-tile plan with that split fits: two launches of 8 rows.

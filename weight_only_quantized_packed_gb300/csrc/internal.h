@@ -69,6 +69,8 @@ cudaError_t launch_w8a16_gemm_tc(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_q2_gemm_tc(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_q2_gemm_mma(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_q2_gemm_stream(const GemvArgs& a, cudaStream_t s);
+// Whether the persistent Q2_0 kernel has a plan for the shape (N, K, device).
+bool q2_gemm_stream_fits(const GemvArgs& a);
 cudaError_t launch_w4a16_gemm_tc(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_w8a16_gemm_mma(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_w4a16_gemm_mma(const GemvArgs& a, cudaStream_t s);
