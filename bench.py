@@ -360,12 +360,7 @@ def sweep(l2, peak, sm_count, f_mhz, bf16_tflops):
                             "compute_view": compute_view(fmt, tc, N, K, M, us, sm_count, f_mhz, bf16_tflops)})
             w.free()
             torch.cuda.empty_cache()
-        # Decoder-layer sequence: qkv, o, gate+up, down, 8 layers cycled.
-        layer = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
-        ws = [Workload("q2", N, K, (1, 4, 8, 16), 0, 4, cap_bytes=0) for (N, K) in layer]
-        for w in ws:
-            w.nbuf = 8
-            w.W = [w.W[0]] + [w.W[0].clone() for _ in range(7)]
+        ws = layer_workloads((1, 4, 8, 16))
         lb = sum(w.wb for w in ws)
         for path, M in [(p, M) for p in (True, "mma") for M in (1, 4, 8, 16)]:
             us = time_calls(lambda: [w.call(M, tc=path) for w in ws], 40)
@@ -679,23 +674,49 @@ def reference_arm(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+# The Q2_0 decoder layer of the sweep: qkv, o, gate+up and down (N, K).
+Q2_LAYER = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
+
+
+def layer_workloads(Ms):
+    """The four projections of a Q2_0 decoder layer, 8 layers' weights
+    cycled (702 MB, past L2): one generated buffer per shape and 7 copies."""
+    ws = [Workload("q2", N, K, Ms, 0, 4, cap_bytes=0) for (N, K) in Q2_LAYER]
+    for w in ws:
+        w.nbuf = 8
+        w.W = [w.W[0]] + [w.W[0].clone() for _ in range(7)]
+    return ws
+
+
 def profile_case(case, launches, pdl):
-    """A fixed number of launches of one call shape, for ncu captures."""
+    """A fixed number of launches of one call shape (fmt:M:N:K[:tc|:mma]),
+    or of decoder-layer passes (layer:M[:tc|:mma], four calls each), for ncu
+    captures."""
     import torch
 
     import weight_only_quantized_packed_gb300 as wqp
 
     parts = case.split(":")
-    fmt, M, N, K = parts[0], int(parts[1]), int(parts[2]), int(parts[3])
-    tc = {"tc": True, "mma": "mma"}.get(parts[4], False) if len(parts) > 4 else False
     wqp.set_pdl(bool(pdl))
-    # About 192 MiB of cycled weights: past L2 (129 MB), well under 1 GiB on the device.
-    w = Workload(fmt, N, K, (M,), 64 << 20, 9, tc=tc, cap_bytes=1 << 30)
-    for _ in range(launches):
-        w.call(M)
+    if parts[0] == "layer":
+        M = int(parts[1])
+        tc = {"tc": True, "mma": "mma"}.get(parts[2], False) if len(parts) > 2 else False
+        ws = layer_workloads((M,))
+        for _ in range(launches):
+            for w in ws:
+                w.call(M, tc=tc)
+        nbuf = ws[0].nbuf
+    else:
+        fmt, M, N, K = parts[0], int(parts[1]), int(parts[2]), int(parts[3])
+        tc = {"tc": True, "mma": "mma"}.get(parts[4], False) if len(parts) > 4 else False
+        # About 192 MiB of cycled weights: past L2 (129 MB), well under 1 GiB on the device.
+        w = Workload(fmt, N, K, (M,), 64 << 20, 9, tc=tc, cap_bytes=1 << 30)
+        for _ in range(launches):
+            w.call(M)
+        nbuf = w.nbuf
     torch.cuda.synchronize()
     err = wqp.get_device_error()
-    print(json.dumps({"case": case, "launches": launches, "buffers": w.nbuf, "device_error": err}))
+    print(json.dumps({"case": case, "launches": launches, "buffers": nbuf, "device_error": err}))
     if err:
         sys.exit(1)
 
@@ -713,7 +734,8 @@ def main():
     ap.add_argument("--reps", type=int, default=7, help="timed regions of --steps steps; the median is reported")
     ap.add_argument("--case", default=None,
                     help="profiling mode: run --launches calls of one shape, fmt:M:N:K[:tc|:mma] "
-                         "(fmt q2|w4|w8), weights cycled past L2; prints one status line")
+                         "(fmt q2|w4|w8), or --launches Q2_0 decoder-layer passes, layer:M[:tc|:mma]; "
+                         "weights cycled past L2; prints one status line")
     ap.add_argument("--launches", type=int, default=6)
     args = ap.parse_args()
     if args.case:
