@@ -100,6 +100,8 @@ S = ctypes.c_void_p(0)
     ((P16, P16b, NUL, P16c, 1, 0, 128, S), "N<1"),
     ((P16, P16b, NUL, P16c, 1, 8, 100, S), "K%128"),
     ((P16, P16b, NUL, P16c, 1, 8, 0, S), "K=0"),
+    ((P16, P16b, NUL, P16c, 1, 8, (1 << 20) + 128, S), "K>2^20"),
+    ((P16, P16b, NUL, P16c, 1, (1 << 24) + 1, 128, S), "N>2^24"),
     ((NUL, P16b, NUL, P16c, 1, 8, 128, S), "A NULL"),
     ((P16, NUL, NUL, P16c, 1, 8, 128, S), "W NULL"),
     ((P16, P16b, NUL, NUL, 1, 8, 128, S), "C NULL"),
@@ -111,6 +113,18 @@ S = ctypes.c_void_p(0)
 def test_q2_validation(L, args, why):
     assert L.q2_gemv(*args) == 1, why
     assert L.wqp_last_error().decode(), why
+
+
+@pytest.mark.parametrize("name", ["q2_gemm_tc", "q2_gemm_mma"])
+def test_largest_shapes_accepted_and_one_past_rejected(L, name):
+    """The limits K <= 2^20 and N <= 2^24 on the tensor-core entries: one
+    past each is rejected before any CUDA call (the largest K itself runs on
+    the GPU in the long-K parity tests)."""
+    f = getattr(L, name)
+    assert f(P16, P16b, P16c, 1, 8, (1 << 20) + 1024, S) == 1
+    assert b"2^20" in L.wqp_last_error()
+    assert f(P16, P16b, P16c, 1, (1 << 24) + 1, 1024, S) == 1
+    assert b"2^24" in L.wqp_last_error()
 
 
 def test_validation_other_formats(L):
