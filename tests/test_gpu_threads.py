@@ -1,12 +1,16 @@
-"""Calls from several host threads at once (GPU needed).
+"""The library's host-side state under concurrent and many-buffer use (GPU
+needed).
 
-The C ABI states that every entry point may be called from several host
-threads. The library keeps process-wide state that the first call of a
-shape fills in: launch plans, encoded tensor maps, occupancy queries and the
-shared-memory attributes of each kernel. Here several threads, each with its
-own CUDA stream, inputs and outputs, start together on shapes no other test
-uses, so they race to fill those entries; every result must equal the same
-call made alone afterwards, bit for bit.
+The library keeps process-wide state that the first call of a shape or a
+weight buffer fills in: launch plans, encoded tensor maps (keyed by address,
+shape, pitch and box), occupancy queries and the shared-memory attributes of
+each kernel.
+* Several host threads, each with its own CUDA stream, inputs and outputs,
+  start together on shapes no other test uses, so they race to fill those
+  entries; every result must equal the same call made alone, bit for bit.
+* More weight buffers than a model's layers would give, called in turn, and
+  a buffer freed and replaced at the same address by one of another shape:
+  every result against the oracle.
 """
 from __future__ import annotations
 
@@ -73,3 +77,34 @@ def test_threads_race_on_first_calls():
         for j, (fmt, eng, N, K) in enumerate(CASES):
             alone = G.host_bits(G.run_gpu(inputs[i][j], tc=eng))
             assert np.array_equal(alone, results[i][j]), (i, fmt, eng, N)
+
+
+# Engines held to the scalar term whose weight maps come from each cache path:
+# the scalar kernel's row map, a 2-D map (Q2_0 warp-level MMA; W4 tcgen05 with
+# its scale map) and a 3-D map (FP8 warp-level MMA).
+@pytest.mark.parametrize("fmt,eng", [("q2", False), ("q2", "mma"), ("w4", True), ("w8", "mma")])
+def test_many_weight_buffers_and_reused_addresses(oracle_lib, fmt, eng):
+    from tests._tol import assert_scalar_term
+
+    N, K, M, count = 96, 1024, 3, 300
+    base = G.make(fmt, M, N, K, seed=1100)
+    ref = G.run_oracle(oracle_lib, base)
+    bufs = [dict(base, dW=G.dev_u8(base["W"])) for _ in range(count)]   # 300 distinct addresses
+    first = None
+    for rnd in range(2):
+        for d in bufs:
+            C = G.host_bits(G.run_gpu(d, tc=eng))
+            if first is None:
+                first = C
+                assert_scalar_term(C, ref, K, f"{fmt} {eng} many buffers")
+            assert np.array_equal(C, first), (fmt, eng, rnd)
+    del bufs, d
+    torch.cuda.synchronize()
+    # Freed blocks come back at the same addresses; a different shape there
+    # must not reuse the earlier maps.
+    other = G.make(fmt, M, N + 32, K, seed=1101)
+    ref2 = G.run_oracle(oracle_lib, other)
+    for _ in range(4):
+        d = dict(other, dW=G.dev_u8(other["W"]))
+        C = G.host_bits(G.run_gpu(d, tc=eng))
+        assert_scalar_term(C, ref2, K, f"{fmt} {eng} reused address")

@@ -326,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, (ScalarCfg<F, M, ARES>::kMinBlocks))
 
 // Host: tensor map of the activation rows, viewed as u32 pairs of BF16.
 cudaError_t make_act_map(CUtensorMap* m, const GemvArgs& a, int box_k);
-// Host: 2-D tensor map (rows x bytes) helper shared by the format traits.
+// Host: 2-D tensor map (rows x bytes) of a weight or scale block, shared by
+// the format traits; cached per process like the tensor-core engines' maps.
 cudaError_t make_rows_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
                           uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
 
