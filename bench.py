@@ -472,6 +472,7 @@ def gpu_arm(args, rank, world, local_rank):
     # the three activation blocks in, compute, copy the three outputs back.
     e2e = e2e_arm(w, H, max(20, min(args.steps, 2000)))
     e2e["value"] = round(e2e["value"] * world, 2)
+    host_us = host_call_us(w, H)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -490,6 +491,7 @@ def gpu_arm(args, rank, world, local_rank):
         "us_per_call": {str(M): round(avg[M], 3) for M in H["Ms"]},
         "pct_of_peak": round(100 * value / world / peak, 2),
         "roofline": roofline, "e2e": e2e,
+        "host_us_per_call": host_us,
         "gpu_launches": args.steps * len(H["Ms"]),
         "clocks": clk_sum,
     }
@@ -500,6 +502,28 @@ def gpu_arm(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
     return line
+
+
+def host_call_us(w, H, n=400):
+    """Host time to issue one call through the public Python API (argument
+    marshalling, the C call's checks, plan and tensor-map lookups and the
+    launch), per M of the step: n calls issued back to back without waiting,
+    so the GPU, at about 4 us per call, keeps the launch queue short."""
+    import torch
+
+    out = {}
+    for M in H["Ms"]:
+        for _ in range(20):
+            w.call(M, tc=H["tc"][M])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            w.call(M, tc=H["tc"][M])
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        out[str(M)] = round((t1 - t0) / n * 1e6, 2)
+    out["how"] = f"{n} back-to-back calls per M through the Python binding, host wall time per call"
+    return out
 
 
 def e2e_arm(w, H, steps):

@@ -71,6 +71,8 @@ class WqpError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """Load libwqp.so (built in-tree by ``__graft_entry__.build()``)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(lib_path):
@@ -100,22 +102,33 @@ def _check(status: int, where: str):
         raise WqpError(status, where, lib().wqp_last_error().decode())
 
 
-def _stream(stream):
-    import torch
+_current_stream = None   # () -> raw handle of this thread's current stream, set on first use
+_BF16 = None
 
+
+def _stream(stream):
+    """The stream argument as an integer handle (ctypes converts it)."""
+    global _current_stream
     if stream is None:
-        # The current stream's raw handle; torch.cuda.current_stream() builds
-        # a Python stream object, which costs about as much host time as a
-        # launch.
-        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
-        if raw is not None:
-            return ctypes.c_void_p(raw(torch._C._cuda_getDevice()))
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        if _current_stream is None:
+            import torch
+
+            # The current stream's raw handle; torch.cuda.current_stream()
+            # builds a Python stream object, which costs about as much host
+            # time as a launch.
+            raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+            if raw is not None:
+                dev = torch._C._cuda_getDevice
+                _current_stream = lambda: raw(dev())
+            else:
+                _current_stream = lambda: torch.cuda.current_stream().cuda_stream
+        return _current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+    """A tensor's device address as an integer (None for no tensor)."""
+    return t.data_ptr() if t is not None else None
 
 
 def _need_cuda(*ts):
@@ -133,7 +146,12 @@ def _out(A, M, N, out):
 
 
 def _rows(A, K):
-    if A.dtype.__repr__() != "torch.bfloat16":
+    global _BF16
+    if _BF16 is None:
+        import torch
+
+        _BF16 = torch.bfloat16
+    if A.dtype is not _BF16:
         raise TypeError("A must be torch.bfloat16")
     if A.dim() != 2 or A.shape[1] != K or A.stride(1) != 1:
         raise ValueError(f"A must be [M, {K}] with unit column stride")
