@@ -599,3 +599,18 @@ def test_largest_k_every_engine(oracle_lib, fmt):
     for eng in (True, "mma"):
         C = G.host_bits(G.run_gpu(d, tc=eng))
         _check_tc(oracle_lib, d, C, f"{fmt} {eng} K={K}")
+
+
+# ------------------------------------------------- fewer rows than one tile
+@pytest.mark.parametrize("fmt,eng,K", [("q2", True, 1024), ("q2", "mma", 1024), ("w4", True, 256), ("w4", "mma", 1024),
+                                       ("w8", True, 1024), ("w8", "mma", 1024)])
+def test_tc_fewer_rows_than_a_tile(oracle_lib, fmt, eng, K):
+    """N = 1, 15 and 17 (less than one 16-row MMA tile, and just over) at
+    the smallest K each engine accepts, M = 1 and 16: the rows past N of the
+    engine's tile are never stored, and every stored output meets its term."""
+    for N in (1, 15, 17):
+        for M in (1, 16):
+            d = G.make(fmt, M, N, K, seed=990 + N + M)
+            C = G.host_bits(G.run_gpu(d, tc=eng))
+            assert C.shape == (M, N)
+            _check_tc(oracle_lib, d, C, f"{fmt} {eng} N={N} M={M} K={K}")
