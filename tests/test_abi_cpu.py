@@ -189,3 +189,38 @@ def test_product_package_does_not_import_oracle():
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, f
                 assert "liboracle" not in txt, f
+
+
+def test_missing_library_and_host_tensors_fail_loudly():
+    """No fallback: without libwqp.so every entry raises ImportError, and
+    host (CPU) tensors are refused before any call. Run in a child process
+    so that this process keeps its loaded library."""
+    import subprocess
+    import sys
+    import textwrap
+
+    code = textwrap.dedent(f"""
+        import sys
+        sys.path.insert(0, {ROOT!r})
+        import torch
+        from weight_only_quantized_packed_gb300 import binding as B
+        A = torch.zeros((1, 1024), dtype=torch.bfloat16)
+        W = torch.zeros((16, 272), dtype=torch.uint8)
+        for f in (lambda: B.q2_gemm_mma(A, W, 16, 1024), lambda: B.q2_gemv(A, W, 16, 1024)):
+            try:
+                f()
+                print("computed")
+            except ValueError as e:
+                print("refused" if "no CPU fallback" in str(e) else "other: " + str(e))
+        B.lib_path = {os.path.join(ROOT, "no_such_dir", "libwqp.so")!r}
+        B._lib = None
+        for f in (B.lib, lambda: B.set_pdl(True), B.get_device_error):
+            try:
+                f()
+                print("loaded")
+            except ImportError:
+                print("importerror")
+    """)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split() == ["refused", "refused", "importerror", "importerror", "importerror"], r.stdout
